@@ -1,0 +1,912 @@
+// Host runtime of the verify-pass library: the C ABI of include/spec.h.
+//
+// A handle owns the packed weights, the target and draft KV caches (paged,
+// 64 positions per page, identity block table over a pool sized for
+// max_ctx), the activation and scratch buffers, and a small device state
+// block with the cache lengths.  Every pass is a fixed sequence of kernel
+// launches on the handle's stream with programmatic dependent launch; kernels
+// read positions from the device state, so no host value changes between
+// steps and a decode loop needs no host round trip.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "spec.h"
+
+using namespace sv;
+
+namespace {
+
+thread_local std::string g_err;
+
+spec_status fail(spec_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+#define CU(call)                                                                                       \
+    do {                                                                                               \
+        cudaError_t e_ = (call);                                                                       \
+        if (e_ != cudaSuccess)                                                                         \
+            return fail(e_ == cudaErrorMemoryAllocation ? SPEC_ERR_OOM : SPEC_ERR_CUDA, "%s: %s (%s:%d)", #call, \
+                        cudaGetErrorString(e_), __FILE__, __LINE__);                                   \
+    } while (0)
+
+enum PassMode { PASS_VERIFY, PASS_DRAFT, PASS_PREFILL_LAST, PASS_PREFILL_MID };
+
+struct LayerW {
+    bool moe = false;
+    PackedMat qkv, o, gu, down;         // dense FFN in gu/down
+    PackedMat router, sgu, sdown;       // MoE
+    PackedMat egu, edown;               // geometry of one expert; experts at a fixed stride
+    long long egu_stride = 0, edown_stride = 0;
+    uint16_t* attn_norm = nullptr;
+    uint16_t* ffn_norm = nullptr;
+};
+
+}  // namespace
+
+struct spec_model {
+    spec_model_config c{};
+    cudaStream_t stream = nullptr;
+    int device = 0, num_sms = 0;
+    bool pdl = true;
+    std::vector<LayerW> L;
+    PackedMat lm;
+    uint16_t* embed = nullptr;
+    uint16_t* final_norm = nullptr;
+    float2* rope = nullptr;
+    int max_pages = 0, nch = 0;
+    int* block_table = nullptr;
+    size_t pool_elems = 0;              // elements of one layer's K (or V) pool
+    uint16_t *kt = nullptr, *vt = nullptr, *kd = nullptr, *vd = nullptr;
+    std::vector<int> plan_full, plan_draft;
+    float* x = nullptr;
+    uint8_t *xf_norm = nullptr, *xf_o = nullptr, *xf_down = nullptr, *xs = nullptr, *xe = nullptr;
+    long long xe_stride = 0;
+    uint16_t* qbuf = nullptr;
+    float* ss = nullptr;
+    float* attn_o = nullptr;
+    float2* attn_ml = nullptr;
+    float* gpart = nullptr;
+    int* gcnt = nullptr;
+    int max_T = 0;
+    float* amax_val = nullptr;
+    int* amax_idx = nullptr;
+    int* route_ids = nullptr;
+    float* route_gates = nullptr;
+    int* forced = nullptr;
+    bool forced_on = false;
+    float* y_slot = nullptr;
+    float* ys = nullptr;
+    DevState* st = nullptr;
+    int moe_mode = SPEC_MOE_DEDUP;
+    int host_len[2] = {0, 0};   // upper bounds of the device lengths
+    bool len_exact[2] = {true, true};
+    int launches = 0;
+    bool profiling = false;
+    struct ProfRec {
+        cudaEvent_t a, b;
+        double bytes;
+    };
+    std::vector<ProfRec> prof;
+    std::vector<void*> allocs;
+    std::vector<void*> draft_allocs;
+};
+
+namespace {
+
+spec_status dalloc(spec_model* h, void** p, size_t bytes, std::vector<void*>* owner = nullptr) {
+    if (bytes == 0) bytes = 16;
+    cudaError_t e = cudaMalloc(p, bytes);
+    if (e != cudaSuccess) return fail(SPEC_ERR_OOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+    (owner ? *owner : h->allocs).push_back(*p);
+    e = cudaMemsetAsync(*p, 0, bytes, h->stream);
+    if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return SPEC_OK;
+}
+
+template <class T>
+spec_status dalloc_t(spec_model* h, T** p, size_t count, std::vector<void*>* owner = nullptr) {
+    return dalloc(h, reinterpret_cast<void**>(p), count * sizeof(T), owner);
+}
+
+PackedMat geometry(int N, int K) {
+    PackedMat m;
+    m.N = N;
+    m.K = K;
+    m.T = (N + kTileRows - 1) / kTileRows;
+    m.KBs = K / kKBlock;
+    return m;
+}
+
+spec_status pack_into(spec_model* h, PackedMat& m, const PackSrc& src) {
+    CU(launch_pack(src, m, h->stream));
+    if (m.T > h->max_T) h->max_T = m.T;
+    return SPEC_OK;
+}
+
+spec_status alloc_packed(spec_model* h, PackedMat& m, int N, int K) {
+    m = geometry(N, K);
+    spec_status s = dalloc(h, reinterpret_cast<void**>(&m.p), m.bytes());
+    if (m.T > h->max_T) h->max_T = m.T;
+    return s;
+}
+
+PackSrc src_rows(std::initializer_list<const void*> ptrs, std::initializer_list<int> rows, int cols, int mode) {
+    PackSrc s{};
+    int i = 0;
+    for (const void* p : ptrs) s.src[i++] = static_cast<const uint16_t*>(p);
+    i = 0;
+    for (int r : rows) s.rows[i++] = r;
+    s.nsrc = i;
+    s.cols = cols;
+    s.mode = mode;
+    return s;
+}
+
+spec_status copy_vec(spec_model* h, uint16_t** dst, const void* src, size_t count) {
+    spec_status s = dalloc_t(h, dst, count);
+    if (s != SPEC_OK) return s;
+    CU(cudaMemcpyAsync(*dst, src, count * 2, cudaMemcpyDeviceToDevice, h->stream));
+    return SPEC_OK;
+}
+
+spec_status validate_config(const spec_model_config* c) {
+    if (!c) return fail(SPEC_ERR_INVALID_ARG, "null config");
+    if (c->n_layers < 1 || c->d_model < 128 || c->d_model % 128) return fail(SPEC_ERR_INVALID_ARG, "d_model must be a positive multiple of 128");
+    if (c->head_dim != 64 && c->head_dim != 128) return fail(SPEC_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+    if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads || c->n_heads / c->n_kv_heads > 4)
+        return fail(SPEC_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads with at most 4 per kv head");
+    if ((c->n_heads * c->head_dim) % 64) return fail(SPEC_ERR_INVALID_ARG, "n_heads*head_dim must be a multiple of 64");
+    if (c->vocab < 1) return fail(SPEC_ERR_INVALID_ARG, "vocab must be positive");
+    if (c->max_ctx < 1 || c->max_ctx > 65536) return fail(SPEC_ERR_INVALID_ARG, "max_ctx must be in 1..65536");
+    if (!(c->norm_eps > 0.f) || !(c->rope_theta > 1.f)) return fail(SPEC_ERR_INVALID_ARG, "bad norm_eps or rope_theta");
+    const bool has_dense = c->n_experts == 0 || c->first_moe_layer > 0;
+    if (has_dense && (c->ffn_dim < 64 || c->ffn_dim % 64)) return fail(SPEC_ERR_INVALID_ARG, "ffn_dim must be a positive multiple of 64");
+    if (c->n_experts < 0 || c->n_experts > kMaxExperts) return fail(SPEC_ERR_INVALID_ARG, "n_experts must be in 0..64");
+    if (c->n_experts > 0) {
+        if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->n_experts) return fail(SPEC_ERR_INVALID_ARG, "top_k must be in 1..min(8, n_experts)");
+        if (c->expert_ffn < 64 || c->expert_ffn % 64) return fail(SPEC_ERR_INVALID_ARG, "expert_ffn must be a positive multiple of 64");
+        if (c->n_shared_experts < 0 || c->n_shared_experts > 2) return fail(SPEC_ERR_INVALID_ARG, "n_shared_experts must be 0..2");
+        if (c->first_moe_layer < 0) return fail(SPEC_ERR_INVALID_ARG, "first_moe_layer must be >= 0");
+    }
+    return SPEC_OK;
+}
+
+spec_status validate_plan(const spec_model* h, const int32_t* layers, int32_t n) {
+    if (n == 0) return SPEC_OK;
+    if (!layers || n < 0 || n > h->c.n_layers) return fail(SPEC_ERR_INVALID_ARG, "bad draft plan size");
+    for (int i = 0; i < n; ++i) {
+        if (layers[i] < 0 || layers[i] >= h->c.n_layers) return fail(SPEC_ERR_INVALID_ARG, "draft layer %d out of range", layers[i]);
+        if (i && layers[i] <= layers[i - 1]) return fail(SPEC_ERR_INVALID_ARG, "draft layers must increase");
+    }
+    if (layers[0] != 0 || layers[n - 1] != h->c.n_layers - 1)
+        return fail(SPEC_ERR_INVALID_ARG, "draft plan must keep the first and the last layer");
+    return SPEC_OK;
+}
+
+spec_status alloc_draft(spec_model* h, const int32_t* layers, int32_t n) {
+    for (void* p : h->draft_allocs) cudaFree(p);
+    h->draft_allocs.clear();
+    h->kd = h->vd = nullptr;
+    h->plan_draft.assign(layers, layers + n);
+    if (n > 0) {
+        spec_status s;
+        if ((s = dalloc_t(h, &h->kd, h->pool_elems * n, &h->draft_allocs)) != SPEC_OK) return s;
+        if ((s = dalloc_t(h, &h->vd, h->pool_elems * n, &h->draft_allocs)) != SPEC_OK) return s;
+    }
+    h->host_len[1] = 0;
+    h->len_exact[1] = true;
+    return SPEC_OK;
+}
+
+// Refresh the host's view of the device lengths (synchronises the stream).
+spec_status sync_lengths(spec_model* h) {
+    CU(cudaStreamSynchronize(h->stream));
+    DevState st;
+    CU(cudaMemcpy(&st, h->st, sizeof(st), cudaMemcpyDeviceToHost));
+    h->host_len[0] = st.len[0];
+    h->host_len[1] = st.len[1];
+    h->len_exact[0] = h->len_exact[1] = true;
+    return SPEC_OK;
+}
+
+spec_status check_capacity(spec_model* h, int which, int n) {
+    if (h->host_len[which] + n <= h->c.max_ctx) return SPEC_OK;
+    if (!h->len_exact[which]) {
+        spec_status s = sync_lengths(h);
+        if (s != SPEC_OK) return s;
+        if (h->host_len[which] + n <= h->c.max_ctx) return SPEC_OK;
+    }
+    return fail(SPEC_ERR_CAPACITY, "cache %d holds %d positions; %d more exceed max_ctx %d", which, h->host_len[which], n,
+                h->c.max_ctx);
+}
+
+GemmParams base_params(spec_model* h, int which, int n) {
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.n = n;
+    p.st = h->st;
+    p.which = which;
+    p.partials = h->gpart;
+    p.counters = h->gcnt;
+    p.d = h->c.d_model;
+    p.norm_eps = h->c.norm_eps;
+    p.ss_in = h->ss;
+    p.ss_in_tiles = h->c.d_model / kTileRows;
+    p.ss_out = h->ss;
+    p.x = h->x;
+    p.n_heads = h->c.n_heads;
+    p.n_kv_heads = h->c.n_kv_heads;
+    p.head_dim = h->c.head_dim;
+    p.n_experts = h->c.n_experts;
+    p.top_k = h->c.top_k;
+    p.moe_mode = h->moe_mode;
+    return p;
+}
+
+void set_mat(GemmParams& p, const PackedMat& m, const uint8_t* X, int epi, int grid_cap) {
+    p.W = m.p;
+    p.T = m.T;
+    p.KBs = m.KBs;
+    p.N = m.N;
+    p.X = X;
+    p.epi = epi;
+    p.items_mode = 0;
+    const long long I = (long long)m.T * m.KBs;
+    p.grid = (int)(I < grid_cap ? I : grid_cap);
+}
+
+// Algorithmic bytes of one dense GEMM launch: weights once, the activation
+// operand once, the outputs once (fp32 residual read+write for EPI_RESID).
+double gemm_bytes(const GemmParams& p) {
+    const double w = (double)p.N * p.KBs * kKBlock * 2.0;
+    const double xin = (double)p.n * p.KBs * kKBlock * 2.0;
+    double out = 0.0;
+    switch (p.epi) {
+        case EPI_QKV: out = (double)p.n * p.N * 2.0; break;
+        case EPI_RESID: out = (double)p.n * p.N * (4.0 + 4.0 + 2.0); break;
+        case EPI_SWIGLU: out = (double)p.n * (p.N / 2) * 2.0; break;
+        case EPI_LMHEAD: out = p.logits ? (double)p.n * p.N * 4.0 : (double)p.n * p.T * 8.0; break;
+        case EPI_STORE: out = (double)p.n * p.N * 4.0; break;
+        default: out = 0.0;
+    }
+    return w + xin + out;
+}
+
+spec_status gemm(spec_model* h, const GemmParams& p) {
+    const bool rec = h->profiling && !p.items_mode;
+    spec_model::ProfRec r{};
+    if (rec) {
+        CU(cudaEventCreate(&r.a));
+        CU(cudaEventCreate(&r.b));
+        CU(cudaEventRecord(r.a, h->stream));
+    }
+    CU(launch_gemm(p, h->stream, h->pdl));
+    ++h->launches;
+    if (rec) {
+        CU(cudaEventRecord(r.b, h->stream));
+        r.bytes = gemm_bytes(p);
+        h->prof.push_back(r);
+    }
+    return SPEC_OK;
+}
+
+// One pass of n tokens through a plan (target: all layers; draft: kept layers).
+spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
+                     int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair, int32_t* d_token,
+                     const int32_t* d_block) {
+    const spec_model_config& c = h->c;
+    const std::vector<int>& plan = which == 0 ? h->plan_full : h->plan_draft;
+    const int d = c.d_model, hd = c.head_dim;
+    const int G = h->num_sms;
+    const bool pdl = h->pdl;
+    spec_status s;
+
+    {
+        EmbedParams e{};
+        e.tokens = d_tokens;
+        e.embed = h->embed;
+        e.n = n;
+        e.d = d;
+        e.vocab = c.vocab;
+        e.x = h->x;
+        e.g_next = h->L[plan[0]].attn_norm;
+        e.xf_out = h->xf_norm;
+        e.ss_out = h->ss;
+        e.st = h->st;
+        CU(launch_embed(e, h->stream, pdl));
+        ++h->launches;
+    }
+    if (d_ids) CU(cudaMemsetAsync(d_ids, 0xFF, sizeof(int32_t) * (size_t)c.n_layers * n * (c.top_k > 0 ? c.top_k : 1), h->stream));
+
+    for (size_t si = 0; si < plan.size(); ++si) {
+        const int l = plan[si];
+        LayerW& W = h->L[l];
+        const uint16_t* g_after = (si + 1 < plan.size()) ? h->L[plan[si + 1]].attn_norm : h->final_norm;
+        uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
+        uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
+
+        // QKV (attn RMSNorm scale, RoPE, paged KV append)
+        GemmParams p = base_params(h, which, n);
+        set_mat(p, W.qkv, h->xf_norm, EPI_QKV, G);
+        p.norm_dim = d;
+        p.rope = h->rope;
+        p.qbuf = h->qbuf;
+        p.kpool = kpool;
+        p.vpool = vpool;
+        p.block_table = h->block_table;
+        if ((s = gemm(h, p)) != SPEC_OK) return s;
+
+        AttnParams a{};
+        a.qbuf = h->qbuf;
+        a.kpool = kpool;
+        a.vpool = vpool;
+        a.block_table = h->block_table;
+        a.part_o = h->attn_o;
+        a.part_ml = h->attn_ml;
+        a.xf_out = h->xf_o;
+        a.st = h->st;
+        a.which = which;
+        a.n = n;
+        a.n_heads = c.n_heads;
+        a.n_kv_heads = c.n_kv_heads;
+        a.head_dim = hd;
+        a.nch = h->nch;
+        a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+        CU(launch_attention(a, h->stream, pdl));
+        h->launches += 2;
+
+        // O projection + residual; next operand = ffn-normed x
+        p = base_params(h, which, n);
+        set_mat(p, W.o, h->xf_o, EPI_RESID, G);
+        p.g_next = W.ffn_norm;
+        p.xf_out = h->xf_norm;
+        if ((s = gemm(h, p)) != SPEC_OK) return s;
+
+        if (!W.moe) {
+            p = base_params(h, which, n);
+            set_mat(p, W.gu, h->xf_norm, EPI_SWIGLU, G);
+            p.norm_dim = d;
+            p.xf_out = h->xf_down;
+            if ((s = gemm(h, p)) != SPEC_OK) return s;
+            p = base_params(h, which, n);
+            set_mat(p, W.down, h->xf_down, EPI_RESID, G);
+            p.g_next = g_after;
+            p.xf_out = h->xf_norm;
+            if ((s = gemm(h, p)) != SPEC_OK) return s;
+        } else {
+            const int K = c.top_k;
+            // router: softmax + top-k
+            p = base_params(h, which, n);
+            set_mat(p, W.router, h->xf_norm, EPI_ROUTER, G);
+            p.norm_dim = d;
+            p.route_ids = h->route_ids;
+            p.route_gates = h->route_gates;
+            p.forced_ids = h->forced_on ? h->forced + (size_t)l * kMaxBlock * K : nullptr;
+            p.debug_ids = (d_ids && which == 0) ? d_ids + (size_t)l * n * K : nullptr;
+            if ((s = gemm(h, p)) != SPEC_OK) return s;
+            // shared experts (dense SwiGLU over all tokens)
+            if (c.n_shared_experts > 0) {
+                p = base_params(h, which, n);
+                set_mat(p, W.sgu, h->xf_norm, EPI_SWIGLU, G);
+                p.norm_dim = d;
+                p.xf_out = h->xs;
+                if ((s = gemm(h, p)) != SPEC_OK) return s;
+            }
+            // routed experts, gate/up: per-slot or deduplicated work items
+            p = base_params(h, which, n);
+            set_mat(p, W.egu, h->xf_norm, EPI_EXPERT_SWIGLU, G);
+            p.items_mode = 1;
+            p.grid = G;
+            p.w_item_stride = W.egu_stride;
+            p.x_item_stride = 0;
+            p.norm_dim = d;
+            p.route_ids = h->route_ids;
+            p.xe = h->xe;
+            p.xe_stride = h->xe_stride;
+            if ((s = gemm(h, p)) != SPEC_OK) return s;
+            if (c.n_shared_experts > 0) {
+                p = base_params(h, which, n);
+                set_mat(p, W.sdown, h->xs, EPI_STORE, G);
+                p.y_store = h->ys;
+                if ((s = gemm(h, p)) != SPEC_OK) return s;
+            }
+            p = base_params(h, which, n);
+            set_mat(p, W.edown, h->xe, EPI_EXPERT_DOWN, G);
+            p.items_mode = 1;
+            p.grid = G;
+            p.w_item_stride = W.edown_stride;
+            p.x_item_stride = h->xe_stride;
+            p.route_ids = h->route_ids;
+            p.y_slot = h->y_slot;
+            if ((s = gemm(h, p)) != SPEC_OK) return s;
+            CombineParams cb{};
+            cb.x = h->x;
+            cb.y_slot = h->y_slot;
+            cb.y_shared = c.n_shared_experts > 0 ? h->ys : nullptr;
+            cb.gates = h->route_gates;
+            cb.n = n;
+            cb.d = d;
+            cb.top_k = K;
+            cb.g_next = g_after;
+            cb.xf_out = h->xf_norm;
+            cb.ss_out = h->ss;
+            CU(launch_moe_combine(cb, h->stream, pdl));
+            ++h->launches;
+        }
+    }
+
+    if (mode == PASS_PREFILL_MID) {
+        CU(launch_advance(h->st, which, n, h->stream, pdl));
+        ++h->launches;
+        return SPEC_OK;
+    }
+    GemmParams p = base_params(h, which, n);
+    set_mat(p, h->lm, h->xf_norm, EPI_LMHEAD, G);
+    p.norm_dim = d;
+    p.logits = d_logits;
+    p.amax_val = h->amax_val;
+    p.amax_idx = h->amax_idx;
+    if ((s = gemm(h, p)) != SPEC_OK) return s;
+
+    AcceptParams ap{};
+    ap.amax_val = h->amax_val;
+    ap.amax_idx = h->amax_idx;
+    ap.T = h->lm.T;
+    ap.n = n;
+    ap.which = which;
+    ap.st = h->st;
+    ap.mode = mode == PASS_VERIFY ? ACC_VERIFY : (mode == PASS_DRAFT ? ACC_DRAFT : ACC_PREFILL);
+    ap.block = d_block;
+    ap.out_argmax = d_argmax;
+    ap.out_accept = d_accept;
+    ap.out_pair = d_pair;
+    ap.out_token = d_token;
+    CU(launch_accept(ap, h->stream, pdl));
+    ++h->launches;
+    return SPEC_OK;
+}
+
+void free_all(spec_model* h) {
+    for (void* p : h->draft_allocs) cudaFree(p);
+    for (void* p : h->allocs) cudaFree(p);
+    h->allocs.clear();
+    h->draft_allocs.clear();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* spec_last_error(void) { return g_err.c_str(); }
+
+spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* w, const int32_t* draft_layers,
+                              int32_t n_draft_layers, void* cuda_stream, spec_handle* out) {
+    if (!out) return fail(SPEC_ERR_INVALID_ARG, "null output handle");
+    *out = nullptr;
+    spec_status s = validate_config(cfg);
+    if (s != SPEC_OK) return s;
+    if (!w || !w->embed || !w->final_norm || !w->layers) return fail(SPEC_ERR_INVALID_ARG, "missing weights");
+    const spec_model_config& c = *cfg;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const spec_layer_weights& lw = w->layers[l];
+        if (!lw.attn_norm || !lw.ffn_norm || !lw.wq || !lw.wk || !lw.wv || !lw.wo)
+            return fail(SPEC_ERR_INVALID_ARG, "layer %d: missing attention weights", l);
+        const bool moe = c.n_experts > 0 && l >= c.first_moe_layer;
+        if (!moe && (!lw.w_gate || !lw.w_up || !lw.w_down)) return fail(SPEC_ERR_INVALID_ARG, "layer %d: missing FFN weights", l);
+        if (moe) {
+            if (!lw.router || !lw.e_gate || !lw.e_up || !lw.e_down) return fail(SPEC_ERR_INVALID_ARG, "layer %d: missing expert weights", l);
+            for (int e = 0; e < c.n_experts; ++e)
+                if (!lw.e_gate[e] || !lw.e_up[e] || !lw.e_down[e]) return fail(SPEC_ERR_INVALID_ARG, "layer %d expert %d: null", l, e);
+            if (c.n_shared_experts > 0) {
+                if (!lw.s_gate || !lw.s_up || !lw.s_down) return fail(SPEC_ERR_INVALID_ARG, "layer %d: missing shared experts", l);
+                for (int e = 0; e < c.n_shared_experts; ++e)
+                    if (!lw.s_gate[e] || !lw.s_up[e] || !lw.s_down[e]) return fail(SPEC_ERR_INVALID_ARG, "layer %d shared %d: null", l, e);
+            }
+        }
+    }
+    if (!c.tied_embeddings && !w->lm_head) return fail(SPEC_ERR_INVALID_ARG, "untied model needs lm_head");
+
+    spec_model* h = new spec_model();
+    h->c = c;
+    h->stream = static_cast<cudaStream_t>(cuda_stream);
+    {
+        spec_status vs = validate_plan(h, draft_layers, n_draft_layers);
+        if (vs != SPEC_OK) {
+            delete h;
+            return vs;
+        }
+    }
+#define TRY(x)                     \
+    do {                           \
+        spec_status t_ = (x);      \
+        if (t_ != SPEC_OK) {       \
+            free_all(h);           \
+            delete h;              \
+            return t_;             \
+        }                          \
+    } while (0)
+#define TRYCU(x) TRY(([&]() -> spec_status { CU(x); return SPEC_OK; })())
+
+    TRYCU(cudaGetDevice(&h->device));
+    cudaDeviceProp prop;
+    TRYCU(cudaGetDeviceProperties(&prop, h->device));
+    if (prop.major != 10 || prop.minor != 3) {
+        std::string msg = "this library is built for sm_103a (GB300); device is sm_" + std::to_string(prop.major) +
+                          std::to_string(prop.minor);
+        delete h;
+        return fail(SPEC_ERR_CUDA, "%s", msg.c_str());
+    }
+    h->num_sms = prop.multiProcessorCount;
+    if (const char* e = std::getenv("SPEC_NO_PDL")) h->pdl = !(e[0] == '1');
+    TRYCU(gemm_configure(h->device));
+    TRYCU(attention_configure(h->device));
+
+    const int d = c.d_model, hd = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads;
+    const int qw = Hq * hd, kw = Hkv * hd;
+    const int S = c.n_experts > 0 ? c.n_shared_experts : 0;
+    const int fe = c.expert_ffn;
+
+    // ---- weights ----
+    TRY(copy_vec(h, &h->embed, w->embed, (size_t)c.vocab * d));
+    TRY(copy_vec(h, &h->final_norm, w->final_norm, d));
+    TRY(alloc_packed(h, h->lm, c.vocab, d));
+    TRY(pack_into(h, h->lm, src_rows({c.tied_embeddings ? w->embed : w->lm_head}, {c.vocab}, d, 0)));
+    h->L.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        const spec_layer_weights& lw = w->layers[l];
+        LayerW& W = h->L[l];
+        W.moe = c.n_experts > 0 && l >= c.first_moe_layer;
+        TRY(copy_vec(h, &W.attn_norm, lw.attn_norm, d));
+        TRY(copy_vec(h, &W.ffn_norm, lw.ffn_norm, d));
+        TRY(alloc_packed(h, W.qkv, qw + 2 * kw, d));
+        TRY(pack_into(h, W.qkv, src_rows({lw.wq, lw.wk, lw.wv}, {qw, kw, kw}, d, 0)));
+        TRY(alloc_packed(h, W.o, d, qw));
+        TRY(pack_into(h, W.o, src_rows({lw.wo}, {d}, qw, 0)));
+        if (!W.moe) {
+            TRY(alloc_packed(h, W.gu, 2 * c.ffn_dim, d));
+            TRY(pack_into(h, W.gu, src_rows({lw.w_gate, lw.w_up}, {c.ffn_dim, c.ffn_dim}, d, 1)));
+            TRY(alloc_packed(h, W.down, d, c.ffn_dim));
+            TRY(pack_into(h, W.down, src_rows({lw.w_down}, {d}, c.ffn_dim, 0)));
+        } else {
+            TRY(alloc_packed(h, W.router, c.n_experts, d));
+            TRY(pack_into(h, W.router, src_rows({lw.router}, {c.n_experts}, d, 0)));
+            // experts: one contiguous region per layer, expert e at e * stride
+            PackedMat g1 = geometry(2 * fe, d), d1 = geometry(d, fe);
+            W.egu_stride = (long long)g1.bytes();
+            W.edown_stride = (long long)d1.bytes();
+            W.egu = g1;
+            W.edown = d1;
+            TRY(dalloc(h, reinterpret_cast<void**>(&W.egu.p), g1.bytes() * c.n_experts));
+            TRY(dalloc(h, reinterpret_cast<void**>(&W.edown.p), d1.bytes() * c.n_experts));
+            if (g1.T > h->max_T) h->max_T = g1.T;
+            if (d1.T > h->max_T) h->max_T = d1.T;
+            for (int e = 0; e < c.n_experts; ++e) {
+                PackedMat ge = g1, de = d1;
+                ge.p = W.egu.p + e * W.egu_stride;
+                de.p = W.edown.p + e * W.edown_stride;
+                TRY(pack_into(h, ge, src_rows({lw.e_gate[e], lw.e_up[e]}, {fe, fe}, d, 1)));
+                TRY(pack_into(h, de, src_rows({lw.e_down[e]}, {d}, fe, 0)));
+            }
+            if (S > 0) {
+                TRY(alloc_packed(h, W.sgu, 2 * S * fe, d));
+                PackSrc ps{};
+                for (int e = 0; e < S; ++e) {
+                    ps.src[e] = static_cast<const uint16_t*>(lw.s_gate[e]);
+                    ps.src[S + e] = static_cast<const uint16_t*>(lw.s_up[e]);
+                    ps.rows[e] = ps.rows[S + e] = fe;
+                }
+                ps.nsrc = 2 * S;
+                ps.cols = d;
+                ps.mode = 1;
+                TRY(pack_into(h, W.sgu, ps));
+                TRY(alloc_packed(h, W.sdown, d, S * fe));
+                PackSrc pd{};
+                for (int e = 0; e < S; ++e) {
+                    pd.src[e] = static_cast<const uint16_t*>(lw.s_down[e]);
+                    pd.rows[e] = d;
+                }
+                pd.nsrc = S;
+                pd.cols = fe;
+                pd.mode = 2;
+                TRY(pack_into(h, W.sdown, pd));
+            }
+        }
+    }
+
+    // ---- caches ----
+    h->nch = (c.max_ctx + kAttnChunk - 1) / kAttnChunk;
+    h->max_pages = h->nch * (kAttnChunk / kPageSize);
+    h->pool_elems = (size_t)h->max_pages * Hkv * kPageSize * hd;
+    TRY(dalloc_t(h, &h->kt, h->pool_elems * c.n_layers));
+    TRY(dalloc_t(h, &h->vt, h->pool_elems * c.n_layers));
+    {
+        std::vector<int> bt(h->max_pages);
+        for (int i = 0; i < h->max_pages; ++i) bt[i] = i;
+        TRY(dalloc_t(h, &h->block_table, h->max_pages));
+        TRYCU(cudaMemcpyAsync(h->block_table, bt.data(), sizeof(int) * bt.size(), cudaMemcpyHostToDevice, h->stream));
+        TRYCU(cudaStreamSynchronize(h->stream));
+    }
+    {
+        // RoPE table, rotate-half pairing: angle = pos * theta^(-2i/hd), in double
+        const int half = hd / 2;
+        std::vector<float2> tab((size_t)c.max_ctx * half);
+        for (int p = 0; p < c.max_ctx; ++p)
+            for (int i = 0; i < half; ++i) {
+                const double ang = (double)p * std::pow((double)c.rope_theta, -2.0 * i / (double)hd);
+                tab[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+            }
+        TRY(dalloc_t(h, &h->rope, tab.size()));
+        TRYCU(cudaMemcpyAsync(h->rope, tab.data(), sizeof(float2) * tab.size(), cudaMemcpyHostToDevice, h->stream));
+        TRYCU(cudaStreamSynchronize(h->stream));
+    }
+    h->plan_full.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) h->plan_full[l] = l;
+    TRY(alloc_draft(h, draft_layers, n_draft_layers));
+
+    // ---- activations and scratch ----
+    const int ffn_max = std::max(c.ffn_dim, 64);
+    TRY(dalloc_t(h, &h->x, (size_t)kMaxBlock * d));
+    TRY(dalloc_t(h, &h->xf_norm, (size_t)(d / kKBlock) * kStageXBytes));
+    TRY(dalloc_t(h, &h->xf_o, (size_t)(qw / kKBlock) * kStageXBytes));
+    TRY(dalloc_t(h, &h->xf_down, (size_t)(ffn_max / kKBlock) * kStageXBytes));
+    TRY(dalloc_t(h, &h->qbuf, (size_t)kMaxBlock * qw));
+    TRY(dalloc_t(h, &h->ss, (size_t)kMaxBlock * (d / kTileRows)));
+    TRY(dalloc_t(h, &h->attn_o, (size_t)Hkv * h->nch * 64 * hd));
+    TRY(dalloc_t(h, &h->attn_ml, (size_t)Hkv * h->nch * 64));
+    TRY(dalloc_t(h, &h->gpart, (size_t)2 * h->num_sms * kTileRows * kMaxBlock));
+    TRY(dalloc_t(h, &h->gcnt, (size_t)h->max_T + 1));
+    TRY(dalloc_t(h, &h->amax_val, (size_t)kMaxBlock * h->lm.T));
+    TRY(dalloc_t(h, &h->amax_idx, (size_t)kMaxBlock * h->lm.T));
+    TRY(dalloc_t(h, &h->st, 1));
+    if (c.n_experts > 0) {
+        const int K = c.top_k;
+        TRY(dalloc_t(h, &h->route_ids, (size_t)kMaxBlock * K));
+        TRY(dalloc_t(h, &h->route_gates, (size_t)kMaxBlock * K));
+        TRY(dalloc_t(h, &h->forced, (size_t)c.n_layers * kMaxBlock * K));
+        TRY(dalloc_t(h, &h->y_slot, (size_t)kMaxBlock * K * d));
+        TRY(dalloc_t(h, &h->ys, (size_t)kMaxBlock * d));
+        TRY(dalloc_t(h, &h->xs, (size_t)(std::max(S, 1) * fe / kKBlock) * kStageXBytes));
+        h->xe_stride = (long long)(fe / kKBlock) * kStageXBytes;
+        TRY(dalloc_t(h, &h->xe, (size_t)h->xe_stride * kMaxBlock * K));
+    }
+    TRYCU(cudaStreamSynchronize(h->stream));
+    TRYCU(cudaGetLastError());
+#undef TRY
+#undef TRYCU
+    *out = h;
+    return SPEC_OK;
+}
+
+spec_status spec_model_destroy(spec_handle h) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    cudaStreamSynchronize(h->stream);
+    free_all(h);
+    delete h;
+    return SPEC_OK;
+}
+
+spec_status spec_set_draft_plan(spec_handle h, const int32_t* draft_layers, int32_t n_draft_layers) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    spec_status s = validate_plan(h, draft_layers, n_draft_layers);
+    if (s != SPEC_OK) return s;
+    CU(cudaStreamSynchronize(h->stream));
+    if ((s = alloc_draft(h, draft_layers, n_draft_layers)) != SPEC_OK) return s;
+    h->launches = 0;
+    CU(launch_rollback(h->st, 1, 0, h->stream, false));
+    CU(cudaStreamSynchronize(h->stream));
+    return SPEC_OK;
+}
+
+spec_status spec_set_stream(spec_handle h, void* cuda_stream) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    h->stream = static_cast<cudaStream_t>(cuda_stream);
+    return SPEC_OK;
+}
+
+spec_status spec_prefill(spec_handle h, const int32_t* d_tokens, int32_t m, int32_t* d_next_token) {
+    if (!h || !d_tokens || !d_next_token || m < 1) return fail(SPEC_ERR_INVALID_ARG, "bad prefill arguments");
+    spec_status s;
+    if ((s = check_capacity(h, 0, m)) != SPEC_OK) return s;
+    const bool draft = !h->plan_draft.empty();
+    if (draft && (s = check_capacity(h, 1, m)) != SPEC_OK) return s;
+    h->launches = 0;
+    for (int off = 0; off < m; off += kMaxBlock) {
+        const int cn = std::min(kMaxBlock, m - off);
+        const bool last = off + cn == m;
+        s = run_pass(h, 0, d_tokens + off, cn, last ? PASS_PREFILL_LAST : PASS_PREFILL_MID, nullptr, nullptr, nullptr,
+                     nullptr, nullptr, last ? d_next_token : nullptr, nullptr);
+        if (s != SPEC_OK) return s;
+    }
+    h->host_len[0] += m;
+    if (draft) {
+        for (int off = 0; off < m; off += kMaxBlock) {
+            const int cn = std::min(kMaxBlock, m - off);
+            s = run_pass(h, 1, d_tokens + off, cn, PASS_PREFILL_MID, nullptr, nullptr, nullptr, nullptr, nullptr,
+                         nullptr, nullptr);
+            if (s != SPEC_OK) return s;
+        }
+        h->host_len[1] += m;
+    }
+    return SPEC_OK;
+}
+
+spec_status spec_draft_step(spec_handle h, const int32_t* d_tokens, int32_t n, int32_t* d_draft_token) {
+    if (!h || !d_tokens || !d_draft_token) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (n < 1 || n > 2) return fail(SPEC_ERR_INVALID_ARG, "draft step takes 1 or 2 tokens");
+    if (h->plan_draft.empty()) return fail(SPEC_ERR_STATE, "model has no draft plan");
+    spec_status s = check_capacity(h, 1, n);
+    if (s != SPEC_OK) return s;
+    h->launches = 0;
+    s = run_pass(h, 1, d_tokens, n, PASS_DRAFT, nullptr, nullptr, nullptr, nullptr, nullptr, d_draft_token, nullptr);
+    if (s == SPEC_OK) h->host_len[1] += n;
+    return s;
+}
+
+spec_status spec_verify_step(spec_handle h, const int32_t* d_block, int32_t n, int32_t* d_argmax, int32_t* d_accept_len,
+                             float* d_logits_opt, int32_t* d_expert_ids_opt, int32_t* d_next_pair_opt) {
+    if (!h || !d_block || !d_argmax || !d_accept_len) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (n < 1 || n > SPEC_MAX_BLOCK) return fail(SPEC_ERR_INVALID_ARG, "block size %d outside 1..16", n);
+    if (d_expert_ids_opt && h->c.n_experts == 0) return fail(SPEC_ERR_INVALID_ARG, "dense model has no expert ids");
+    spec_status s = check_capacity(h, 0, n);
+    if (s != SPEC_OK) return s;
+    h->launches = 0;
+    s = run_pass(h, 0, d_block, n, PASS_VERIFY, d_argmax, d_accept_len, d_logits_opt, d_expert_ids_opt, d_next_pair_opt,
+                 nullptr, d_block);
+    if (s == SPEC_OK) h->host_len[0] += n;
+    return s;
+}
+
+spec_status spec_kv_rollback(spec_handle h, int32_t which, int32_t new_len) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (which != SPEC_CACHE_TARGET && which != SPEC_CACHE_DRAFT) return fail(SPEC_ERR_INVALID_ARG, "bad cache id");
+    if (which == SPEC_CACHE_DRAFT && h->plan_draft.empty()) return fail(SPEC_ERR_STATE, "model has no draft plan");
+    if (new_len < -1) return fail(SPEC_ERR_INVALID_ARG, "bad length %d", new_len);
+    if (new_len >= 0 && new_len > h->host_len[which]) {
+        spec_status s = h->len_exact[which] ? SPEC_OK : sync_lengths(h);
+        if (s != SPEC_OK) return s;
+        if (new_len > h->host_len[which])
+            return fail(SPEC_ERR_INVALID_ARG, "rollback to %d beyond the %d cached positions", new_len, h->host_len[which]);
+    }
+    h->launches = 0;
+    CU(launch_rollback(h->st, which, new_len, h->stream, h->pdl));
+    h->launches = 1;
+    if (new_len >= 0) {
+        h->host_len[which] = new_len;
+        h->len_exact[which] = true;
+    } else {
+        h->len_exact[which] = false;   // known on the device only; host keeps the upper bound
+    }
+    return SPEC_OK;
+}
+
+spec_status spec_moe_mode(spec_handle h, int32_t mode) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (mode != SPEC_MOE_PER_SLOT && mode != SPEC_MOE_DEDUP) return fail(SPEC_ERR_INVALID_ARG, "bad MoE mode");
+    if (h->c.n_experts == 0) return fail(SPEC_ERR_STATE, "dense model");
+    h->moe_mode = mode;
+    return SPEC_OK;
+}
+
+spec_status spec_check_error(spec_handle h) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    CU(cudaStreamSynchronize(h->stream));
+    CU(cudaGetLastError());
+    int err = 0;
+    CU(cudaMemcpy(&err, &h->st->error, sizeof(int), cudaMemcpyDeviceToHost));
+    if (err) {
+        int zero = 0;
+        CU(cudaMemcpy(&h->st->error, &zero, sizeof(int), cudaMemcpyHostToDevice));
+        CU(cudaMemset(h->gcnt, 0, sizeof(int) * (h->max_T + 1)));
+        return fail(err == 10 ? SPEC_ERR_INVALID_ARG : SPEC_ERR_TIMEOUT,
+                    err == 10 ? "a token id outside [0, vocab) was replaced by 0" : "device error code %d", err);
+    }
+    return SPEC_OK;
+}
+
+spec_status spec_kv_len(spec_handle h, int32_t which, int32_t* out_len) {
+    if (!h || !out_len || (which != 0 && which != 1)) return fail(SPEC_ERR_INVALID_ARG, "bad arguments");
+    spec_status s = sync_lengths(h);
+    if (s != SPEC_OK) return s;
+    *out_len = h->host_len[which];
+    return SPEC_OK;
+}
+
+static spec_status kv_io(spec_handle h, int32_t which, int32_t slot, void* dk, void* dv, int32_t ctx, bool load) {
+    if (!h || !dk || !dv) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (which != 0 && which != 1) return fail(SPEC_ERR_INVALID_ARG, "bad cache id");
+    const int nslots = which == 0 ? h->c.n_layers : (int)h->plan_draft.size();
+    if (slot < 0 || slot >= nslots) return fail(SPEC_ERR_INVALID_ARG, "slot %d out of range", slot);
+    if (ctx < 0 || ctx > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "ctx %d out of range", ctx);
+    uint16_t* kp = (which == 0 ? h->kt : h->kd) + h->pool_elems * slot;
+    uint16_t* vp = (which == 0 ? h->vt : h->vd) + h->pool_elems * slot;
+    CU(launch_kv_io(kp, h->block_table, static_cast<uint16_t*>(dk), ctx, h->c.n_kv_heads, h->c.head_dim, load, h->stream));
+    CU(launch_kv_io(vp, h->block_table, static_cast<uint16_t*>(dv), ctx, h->c.n_kv_heads, h->c.head_dim, load, h->stream));
+    return SPEC_OK;
+}
+
+spec_status spec_kv_load(spec_handle h, int32_t which, int32_t slot, const void* d_k, const void* d_v, int32_t ctx) {
+    return kv_io(h, which, slot, const_cast<void*>(d_k), const_cast<void*>(d_v), ctx, true);
+}
+
+spec_status spec_kv_export(spec_handle h, int32_t which, int32_t slot, void* d_k, void* d_v, int32_t ctx) {
+    return kv_io(h, which, slot, d_k, d_v, ctx, false);
+}
+
+spec_status spec_kv_set_len(spec_handle h, int32_t which, int32_t len) {
+    if (!h || (which != 0 && which != 1)) return fail(SPEC_ERR_INVALID_ARG, "bad arguments");
+    if (len < 0 || len > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "length %d out of range", len);
+    CU(launch_rollback(h->st, which, len, h->stream, false));
+    h->host_len[which] = len;
+    h->len_exact[which] = true;
+    return SPEC_OK;
+}
+
+spec_status spec_moe_force_routing(spec_handle h, const int32_t* d_ids) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (h->c.n_experts == 0) return fail(SPEC_ERR_STATE, "dense model");
+    if (!d_ids) {
+        h->forced_on = false;
+        return SPEC_OK;
+    }
+    const size_t count = (size_t)h->c.n_layers * kMaxBlock * h->c.top_k;
+    std::vector<int32_t> ids(count);
+    CU(cudaStreamSynchronize(h->stream));
+    CU(cudaMemcpy(ids.data(), d_ids, count * sizeof(int32_t), cudaMemcpyDeviceToHost));
+    const int K = h->c.top_k;
+    for (int l = h->c.first_moe_layer; l < h->c.n_layers; ++l)
+        for (int j = 0; j < kMaxBlock; ++j) {
+            const int32_t* r = &ids[((size_t)l * kMaxBlock + j) * K];
+            for (int s = 0; s < K; ++s) {
+                if (r[s] < 0 || r[s] >= h->c.n_experts) return fail(SPEC_ERR_INVALID_ARG, "forced expert id %d out of range", r[s]);
+                for (int t = 0; t < s; ++t)
+                    if (r[t] == r[s]) return fail(SPEC_ERR_INVALID_ARG, "forced ids of a token must be distinct");
+            }
+        }
+    CU(cudaMemcpyAsync(h->forced, ids.data(), count * sizeof(int32_t), cudaMemcpyHostToDevice, h->stream));
+    CU(cudaStreamSynchronize(h->stream));
+    h->forced_on = true;
+    return SPEC_OK;
+}
+
+int32_t spec_last_launch_count(spec_handle h) { return h ? h->launches : -1; }
+
+spec_status spec_profile_enable(spec_handle h, int32_t enable) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    h->profiling = enable != 0;
+    return SPEC_OK;
+}
+
+spec_status spec_profile_read(spec_handle h, double* total_ms, double* total_bytes, int32_t* launches) {
+    if (!h || !total_ms || !total_bytes || !launches) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    CU(cudaStreamSynchronize(h->stream));
+    double ms = 0.0, bytes = 0.0;
+    for (auto& r : h->prof) {
+        float t = 0.f;
+        CU(cudaEventElapsedTime(&t, r.a, r.b));
+        ms += t;
+        bytes += r.bytes;
+        cudaEventDestroy(r.a);
+        cudaEventDestroy(r.b);
+    }
+    *total_ms = ms;
+    *total_bytes = bytes;
+    *launches = (int32_t)h->prof.size();
+    h->prof.clear();
+    return SPEC_OK;
+}
+
+}  // extern "C"

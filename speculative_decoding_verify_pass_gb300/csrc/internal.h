@@ -1,0 +1,160 @@
+// Internal interface between the host runtime (api.cu) and the kernel
+// translation units.  Plain structs of device pointers and sizes, one
+// launcher per kernel family; every launcher enqueues on the given stream with
+// programmatic dependent launch and returns the CUDA error of the launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace sv {
+
+// Epilogue kinds of the streaming GEMM.
+enum EpiKind : int {
+    EPI_QKV = 0,            // rstd scale, RoPE on q/k, q -> qbuf, k/v -> paged cache
+    EPI_RESID = 1,          // x += acc; next-norm operand + sum-of-squares partials
+    EPI_SWIGLU = 2,         // silu(rstd*gate) * (rstd*up) -> next operand
+    EPI_LMHEAD = 3,         // rstd scale, optional logits, per-tile argmax partials
+    EPI_ROUTER = 4,         // softmax over experts, top-k ids and gates
+    EPI_EXPERT_SWIGLU = 5,  // per work item: SwiGLU rows of its tokens -> item operand
+    EPI_EXPERT_DOWN = 6,    // per work item: rows of its tokens -> y_slot
+    EPI_STORE = 7           // acc -> fp32 rows (shared-expert output)
+};
+
+// A weight matrix [N][K] repacked as tiles of 128 rows x 64 k in the order the
+// consumer warps read A fragments: [tile][kblock][m16 (8)][k16 (4)][lane][8 bf16].
+struct PackedMat {
+    uint8_t* p = nullptr;
+    int N = 0, K = 0, T = 0, KBs = 0;
+    size_t bytes() const { return (size_t)T * KBs * kStageWBytes; }
+};
+
+struct GemmParams {
+    const uint8_t* W;          // packed weights (items mode: expert e at W + e*w_item_stride)
+    long long w_item_stride;
+    int T, KBs, N;
+    const uint8_t* X;          // fragment-ordered operand [KBs][2 KB] (items: + item*x_item_stride)
+    long long x_item_stride;
+    int n;                     // tokens (1..16)
+    int items_mode;            // 0: stream-K over T*KBs; 1: (item, tile) units
+    int grid;                  // CTAs launched
+    float* partials;           // stream-K partial tiles [2*grid][128*16]
+    int* counters;             // [T], zero between launches
+    DevState* st;
+    int which;                 // cache whose length gives the positions
+    int epi;
+    // input normalisation (rstd applied in the epilogue)
+    const float* ss_in;        // [16][ss_in_tiles] sum-of-squares partials of x
+    int ss_in_tiles;
+    int norm_dim;              // 0: no normalisation
+    float norm_eps;
+    // EPI_QKV
+    int n_heads, n_kv_heads, head_dim;
+    const float2* rope;        // [max_pos][head_dim/2] (cos, sin)
+    uint16_t* qbuf;            // [16][n_heads*head_dim]
+    uint16_t* kpool;           // this layer's pages [page][n_kv_heads][64][head_dim]
+    uint16_t* vpool;
+    const int* block_table;
+    // EPI_RESID
+    float* x;                  // [16][d]
+    int d;
+    const uint16_t* g_next;    // gain of the norm that consumes x next
+    uint8_t* xf_out;           // next GEMM's operand
+    float* ss_out;             // [16][d/128]
+    // EPI_LMHEAD
+    float* logits;             // optional [n][vocab]
+    float* amax_val;           // [16][T]
+    int* amax_idx;
+    // EPI_ROUTER / experts
+    int n_experts, top_k;
+    int* route_ids;            // [16][top_k]
+    float* route_gates;
+    const int* forced_ids;     // [16][top_k] or null
+    int* debug_ids;            // [n][top_k] or null
+    int moe_mode;
+    float* y_slot;             // [16][top_k][d]
+    float* y_store;            // [16][N] (EPI_STORE)
+    uint8_t* xe;               // expert-down operands [item][KBs_down][2 KB]
+    long long xe_stride;
+};
+
+struct AttnParams {
+    const uint16_t* qbuf;      // [16][Hq*hd]
+    const uint16_t* kpool;     // [page][Hkv][64][hd]
+    const uint16_t* vpool;
+    const int* block_table;
+    float* part_o;             // [Hkv][nch][64][hd]
+    float2* part_ml;           // [Hkv][nch][64] (max (log2 domain), sum)
+    uint8_t* xf_out;           // O-projection operand
+    DevState* st;
+    int which, n, n_heads, n_kv_heads, head_dim, nch;
+    float scale_log2;          // log2(e) / sqrt(hd)
+};
+
+// Launchers (stream, PDL).  Return cudaSuccess or the launch error.
+cudaError_t launch_gemm(const GemmParams& p, cudaStream_t s, bool pdl);
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl);
+cudaError_t gemm_configure(int device);  // shared-memory opt-in, once per device
+cudaError_t attention_configure(int device);
+int gemm_threads();
+size_t gemm_smem_bytes();
+
+struct EmbedParams {
+    const int* tokens;         // device [n]
+    const uint16_t* embed;     // [V][d]
+    int n, d, vocab;
+    float* x;
+    const uint16_t* g_next;
+    uint8_t* xf_out;
+    float* ss_out;
+    DevState* st;
+};
+cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl);
+
+struct CombineParams {           // MoE: x += sum_s gate*y_slot + y_shared
+    float* x;
+    const float* y_slot;
+    const float* y_shared;
+    const float* gates;
+    int n, d, top_k;
+    const uint16_t* g_next;
+    uint8_t* xf_out;
+    float* ss_out;
+};
+cudaError_t launch_moe_combine(const CombineParams& p, cudaStream_t s, bool pdl);
+
+enum AcceptMode : int { ACC_VERIFY = 0, ACC_DRAFT = 1, ACC_PREFILL = 2 };
+struct AcceptParams {
+    const float* amax_val;     // [16][T]
+    const int* amax_idx;
+    int T, n, mode, which;
+    const int* block;          // verify: d_block
+    int* out_argmax;           // verify: [n]
+    int* out_accept;           // verify: [1]
+    int* out_pair;             // verify: [2] or null
+    int* out_token;            // draft / prefill: [1]
+    DevState* st;
+};
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s, bool pdl);
+
+// len[which] += n (a pass without LM head).
+cudaError_t launch_advance(DevState* st, int which, int n, cudaStream_t s, bool pdl);
+// Rollback: new_len >= 0 sets it; -1 applies the device rule of spec_kv_rollback.
+cudaError_t launch_rollback(DevState* st, int which, int new_len, cudaStream_t s, bool pdl);
+
+struct PackSrc {
+    const uint16_t* src[4];
+    int rows[4];               // rows of each source
+    int cols;                  // K of each source (mode 2: columns per source)
+    int nsrc;
+    int mode;                  // 0 row concat, 1 gate/up interleave by 64, 2 column concat
+};
+cudaError_t launch_pack(const PackSrc& s, const PackedMat& m, cudaStream_t st);
+
+// Logical [ctx][Hkv][hd] bf16 <-> paged, swizzled pool.
+cudaError_t launch_kv_io(uint16_t* pool, const int* block_table, uint16_t* logical, int ctx, int hkv, int hd,
+                         bool to_pool, cudaStream_t s);
+
+}  // namespace sv

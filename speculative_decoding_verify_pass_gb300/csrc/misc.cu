@@ -1,0 +1,270 @@
+// Small kernels around the streaming GEMMs: token embedding, MoE combine,
+// argmax reduction + greedy accept, cache-length updates, weight repacking
+// and KV-cache import/export.
+#include <math.h>
+
+#include "internal.h"
+
+namespace sv {
+
+namespace {
+
+cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void** args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Writes row j's 8 values starting at R0 into the residual, the next GEMM's
+// operand (x * gain, bf16, fragment order) and returns their sum of squares.
+__device__ __forceinline__ float store_residual8(float* xr, const float (&v)[8], int j, int R0, const uint16_t* g_next,
+                                                 uint8_t* xf_out) {
+    float ssum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        ssum += v[e] * v[e];
+        const int R = R0 + e;
+        *reinterpret_cast<uint16_t*>(xf_out + (size_t)(R >> 6) * kStageXBytes + xfrag_offset(j, R & 63)) =
+            f2bf(v[e] * bf2f(g_next[R]));
+    }
+    *reinterpret_cast<float4*>(xr) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<float4*>(xr + 4) = make_float4(v[4], v[5], v[6], v[7]);
+    return ssum;
+}
+
+// x[j] = embed[token_j] (bf16 -> fp32); one CTA per 128 columns, 16 threads
+// per token each owning 8 columns.
+__global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ EmbedParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tile = blockIdx.x, tid = threadIdx.x;
+    const int j = tid >> 4, rg = tid & 15;
+    float ssum = 0.f;
+    if (j < p.n) {
+        int tok = p.tokens[j];
+        if (tok < 0 || tok >= p.vocab) {
+            atomicCAS(&p.st->error, 0, 10);
+            tok = 0;
+        }
+        const int R0 = tile * kTileRows + rg * 8;
+        const uint4 raw = *reinterpret_cast<const uint4*>(p.embed + (size_t)tok * p.d + R0);
+        const uint16_t* b = reinterpret_cast<const uint16_t*>(&raw);
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = bf2f(b[e]);
+        ssum = store_residual8(p.x + (size_t)j * p.d + R0, v, j, R0, p.g_next, p.xf_out);
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (rg == 0 && j < p.n) p.ss_out[j * (p.d / kTileRows) + tile] = ssum;
+}
+
+// MoE layer output: x[j] += sum_s gate[j][s] * y_slot[j][s] + y_shared[j],
+// slots in rank order, then the next norm's operand and sum-of-squares.
+__global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant__ CombineParams p) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tile = blockIdx.x, tid = threadIdx.x;
+    const int j = tid >> 4, rg = tid & 15;
+    float ssum = 0.f;
+    if (j < p.n) {
+        const int R0 = tile * kTileRows + rg * 8;
+        float* xr = p.x + (size_t)j * p.d + R0;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float y = 0.f;
+            for (int s = 0; s < p.top_k; ++s)
+                y += p.gates[j * p.top_k + s] * p.y_slot[((size_t)j * p.top_k + s) * p.d + R0 + e];
+            if (p.y_shared) y += p.y_shared[(size_t)j * p.d + R0 + e];
+            v[e] = xr[e] + y;
+        }
+        ssum = store_residual8(xr, v, j, R0, p.g_next, p.xf_out);
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (rg == 0 && j < p.n) p.ss_out[j * (p.d / kTileRows) + tile] = ssum;
+}
+
+// Per-token argmax over the LM head's tile partials (lowest id on ties), then
+// the greedy accept rule and the cache-length bookkeeping.
+__global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ AcceptParams p) {
+    __shared__ int am[kMaxBlock];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < p.n) {
+        float best = -INFINITY;
+        int bi = 0x7fffffff;
+        for (int t = lane; t < p.T; t += 32) {
+            const float v = p.amax_val[warp * p.T + t];
+            const int i = p.amax_idx[warp * p.T + t];
+            if (v > best || (v == best && i < bi)) {
+                best = v;
+                bi = i;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > best || (ov == best && oi < bi)) {
+                best = ov;
+                bi = oi;
+            }
+        }
+        if (lane == 0) am[warp] = bi == 0x7fffffff ? 0 : bi;
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    DevState* st = p.st;
+    const int pos0 = st->len[p.which];
+    if (p.mode == ACC_VERIFY) {
+        int k = 0;
+        while (k < p.n - 1 && p.block[k + 1] == am[k]) ++k;   // cumulative product of matches
+        const int tok_k = p.block[k];
+        for (int j = 0; j < p.n; ++j) p.out_argmax[j] = am[j];
+        *p.out_accept = k;
+        if (p.out_pair) {
+            p.out_pair[0] = tok_k;
+            p.out_pair[1] = am[k];
+        }
+        st->verify_pos = pos0;
+        st->verify_accept = k;
+    } else if (p.out_token) {
+        *p.out_token = am[p.n - 1];
+    }
+    st->len[p.which] = pos0 + p.n;
+}
+
+__global__ void advance_kernel(DevState* st, int which, int n) {
+    pdl_launch_dependents();
+    pdl_wait();
+    st->len[which] += n;
+}
+
+__global__ void rollback_kernel(DevState* st, int which, int new_len) {
+    pdl_launch_dependents();
+    pdl_wait();
+    if (new_len >= 0) {
+        st->len[which] = new_len;
+    } else if (which == 0) {
+        st->len[0] = st->verify_pos + st->verify_accept + 1;
+    } else {
+        const int keep = st->verify_pos + st->verify_accept;
+        if (keep < st->len[1]) st->len[1] = keep;
+    }
+}
+
+// Logical row r of the packed matrix -> source element (or zero).
+__device__ __forceinline__ uint16_t pack_fetch(const PackSrc& s, int N, int r, int k) {
+    if (r >= N) return 0;
+    if (s.mode == 2) {  // column concat: k selects the source
+        const int src = k / s.cols;
+        return s.src[src][(size_t)r * s.cols + (k - src * s.cols)];
+    }
+    int row = r;
+    int first = 0, count = s.nsrc;
+    if (s.mode == 1) {  // tile t rows 0..63 = gate rows t*64.., rows 64..127 = up rows t*64..
+        const int t = r >> 7, i = r & 127;
+        row = t * 64 + (i & 63);
+        first = (i < 64) ? 0 : s.nsrc / 2;
+        count = s.nsrc / 2;
+    }
+    for (int q = first; q < first + count; ++q) {
+        if (row < s.rows[q]) return s.src[q][(size_t)row * s.cols + k];
+        row -= s.rows[q];
+    }
+    return 0;
+}
+
+// One thread per 16-byte A fragment chunk of the packed layout.
+__global__ void pack_kernel(PackSrc s, uint8_t* out, int N, int T, int KBs) {
+    const long long total = (long long)T * KBs * (kStageWBytes / 16);
+    for (long long ch = blockIdx.x * (long long)blockDim.x + threadIdx.x; ch < total;
+         ch += (long long)gridDim.x * blockDim.x) {
+        const int lane = (int)(ch & 31), k16 = (int)((ch >> 5) & 3), m16 = (int)((ch >> 7) & 7);
+        const long long tb = ch >> 10;
+        const int b = (int)(tb % KBs), t = (int)(tb / KBs);
+        const int g = lane >> 2, c = lane & 3;
+        const int r0 = t * kTileRows + m16 * 16 + g, r1 = r0 + 8;
+        const int k0 = b * kKBlock + k16 * 16 + 2 * c, k1 = k0 + 8;
+        uint16_t v[8] = {pack_fetch(s, N, r0, k0), pack_fetch(s, N, r0, k0 + 1), pack_fetch(s, N, r1, k0),
+                         pack_fetch(s, N, r1, k0 + 1), pack_fetch(s, N, r0, k1), pack_fetch(s, N, r0, k1 + 1),
+                         pack_fetch(s, N, r1, k1), pack_fetch(s, N, r1, k1 + 1)};
+        *reinterpret_cast<uint4*>(out + ch * 16) = *reinterpret_cast<const uint4*>(v);
+    }
+}
+
+__global__ void kv_io_kernel(uint16_t* pool, const int* bt, uint16_t* logical, int ctx, int hkv, int hd, int to_pool) {
+    const long long total = (long long)ctx * hkv * hd;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int dim = (int)(i % hd);
+        const int h = (int)((i / hd) % hkv);
+        const int pos = (int)(i / ((long long)hd * hkv));
+        const size_t pi = ((size_t)(bt[pos / kPageSize] * hkv + h) * kPageSize) * hd + kv_swz(pos % kPageSize, dim, hd);
+        if (to_pool)
+            pool[pi] = logical[i];
+        else
+            logical[i] = pool[pi];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl) {
+    EmbedParams q = p;
+    void* args[] = {&q};
+    return launch_ex((const void*)embed_kernel, dim3((unsigned)(p.d / kTileRows)), dim3(256), 0, s, pdl, args);
+}
+
+cudaError_t launch_moe_combine(const CombineParams& p, cudaStream_t s, bool pdl) {
+    CombineParams q = p;
+    void* args[] = {&q};
+    return launch_ex((const void*)moe_combine_kernel, dim3((unsigned)(p.d / kTileRows)), dim3(256), 0, s, pdl, args);
+}
+
+cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s, bool pdl) {
+    AcceptParams q = p;
+    void* args[] = {&q};
+    return launch_ex((const void*)accept_kernel, dim3(1), dim3(512), 0, s, pdl, args);
+}
+
+cudaError_t launch_advance(DevState* st, int which, int n, cudaStream_t s, bool pdl) {
+    void* args[] = {&st, &which, &n};
+    return launch_ex((const void*)advance_kernel, dim3(1), dim3(1), 0, s, pdl, args);
+}
+
+cudaError_t launch_rollback(DevState* st, int which, int new_len, cudaStream_t s, bool pdl) {
+    void* args[] = {&st, &which, &new_len};
+    return launch_ex((const void*)rollback_kernel, dim3(1), dim3(1), 0, s, pdl, args);
+}
+
+cudaError_t launch_pack(const PackSrc& src, const PackedMat& m, cudaStream_t st) {
+    const long long total = (long long)m.T * m.KBs * (kStageWBytes / 16);
+    long long blocks = (total + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    pack_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, m.p, m.N, m.T, m.KBs);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kv_io(uint16_t* pool, const int* bt, uint16_t* logical, int ctx, int hkv, int hd, bool to_pool,
+                         cudaStream_t s) {
+    const long long total = (long long)ctx * hkv * hd;
+    if (total == 0) return cudaSuccess;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    kv_io_kernel<<<(unsigned)blocks, 256, 0, s>>>(pool, bt, logical, ctx, hkv, hd, to_pool ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -53,15 +53,15 @@ static inline uint16_t sv_bf16(float f) {
 void sv_normal_bf16(uint16_t* out, int64_t count, uint64_t seed, uint64_t stream, int64_t first, double stdev) {
     const uint64_t key = sv_key(seed, stream);
     const double two_pi = 6.283185307179586476925286766559;
+    const int64_t p0 = first >> 1, p1 = (first + count + 1) >> 1;
 #pragma omp parallel for schedule(static)
-    for (int64_t k = 0; k < count; ++k) {
-        const int64_t idx = first + k;
-        const int64_t pair = idx >> 1;
+    for (int64_t pair = p0; pair < p1; ++pair) {
         const double u1 = sv_unit(sv_word(key, (uint64_t)(2 * pair)));
         const double u2 = sv_unit(sv_word(key, (uint64_t)(2 * pair + 1)));
         const double r = sqrt(-2.0 * log(u1));
-        const double z = (idx & 1) ? r * sin(two_pi * u2) : r * cos(two_pi * u2);
-        out[k] = sv_bf16((float)(stdev * z));
+        const int64_t i0 = 2 * pair - first, i1 = i0 + 1;
+        if (i0 >= 0 && i0 < count) out[i0] = sv_bf16((float)(stdev * (r * cos(two_pi * u2))));
+        if (i1 >= 0 && i1 < count) out[i1] = sv_bf16((float)(stdev * (r * sin(two_pi * u2))));
     }
 }
 

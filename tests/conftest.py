@@ -50,4 +50,4 @@ def small_gqa_cfg():
     """A small grouped-query model (4 query heads per kv head, tied LM head)."""
     import synth
     return synth.ModelConfig("gqa-small", 3, 256, 8, 2, 64, 512, 1000, rope_theta=5e5,
-                             tied_embeddings=True, max_ctx=256, index=1)
+                             tied_embeddings=True, max_ctx=512, index=1)

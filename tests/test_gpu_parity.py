@@ -1,0 +1,246 @@
+"""GPU parity of the verify pass (C ABI through the binding) against the CPU oracle.
+
+Small models whose oracle runs in seconds but whose matrices still span
+several 128-row tiles, several 64-wide k-blocks, more than one KV page and
+ragged tails (vocab 1000, blocks of 1..16 tokens, contexts off page
+boundaries)."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from conftest import small_gqa_cfg, small_moe_cfg
+from gpu_common import ATOL, RTOL, argmax_mismatches, assert_logits_close, make_model, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module")
+def torch():
+    return torch_cuda()
+
+
+@pytest.fixture(scope="module")
+def tiny_model(torch, tiny_cfg, tiny_weights):
+    return make_model(tiny_cfg, tiny_weights, draft_plan=oracle.layer_skip_plan(tiny_cfg.n_layers, 0.5))
+
+
+def reset(m):
+    import speculative_decoding_verify_pass_gb300 as sv
+    m.kv_set_len(sv.SPEC_CACHE_TARGET, 0)
+    if m.draft_plan:
+        m.kv_set_len(sv.SPEC_CACHE_DRAFT, 0)
+
+
+def test_library_exports_and_launches(torch, tiny_model):
+    import speculative_decoding_verify_pass_gb300 as sv
+    lib = sv.library()
+    for name in sv.EXPORTED:
+        assert hasattr(lib, name)
+    reset(tiny_model)
+    tiny_model.prefill(np.arange(20, dtype=np.int32))
+    assert tiny_model.launches() > 0
+
+
+def test_tiny_prefill_verify_logits_match_oracle(torch, tiny_cfg, tiny_oracle, tiny_model, tiny_prompt):
+    m, orc = tiny_model, tiny_oracle
+    reset(m)
+    p = tiny_prompt
+    nxt = m.prefill(p[:100])
+    oc = orc.new_cache()
+    ol, _, _ = orc.forward(oc, orc.full_plan, p[:100], 0, logits_from=99)
+    argmax_mismatches([int(nxt.item())], ol)
+    for n in (1, 2, 5, 8, 9, 16):
+        block = torch.tensor(p[100:100 + n], dtype=torch.int32, device="cuda")
+        am, acc, lg, _ = m.verify(block, logits=True)
+        ref, _, _ = orc.forward(oc, orc.full_plan, p[100:100 + n], 100)
+        assert_logits_close(lg.cpu().numpy(), ref, "tiny n=%d" % n)
+        argmax_mismatches(am.cpu().numpy(), ref)
+        a = [int(np.argmax(r)) for r in ref]
+        assert int(acc.item()) == oracle.accept_len(p[100:100 + n], a)
+        m.rollback(0, 100)
+        oc.truncate(100)
+
+
+def test_tiny_greedy_matches_golden(torch, tiny_cfg, tiny_model, tiny_prompt):
+    reset(tiny_model)
+    m = make_model(tiny_cfg, tiny_model_weights(tiny_cfg))
+    got = m.greedy(tiny_prompt, 64)
+    want = [int(t) for t in open(os.path.join(GOLDEN, "tiny_greedy.txt")).read().split("\n")[-2].split()]
+    assert got == want
+
+
+_W = {}
+
+
+def tiny_model_weights(cfg):
+    if "tiny" not in _W:
+        _W["tiny"] = synth.make_weights(cfg)
+    return _W["tiny"]
+
+
+@pytest.mark.parametrize("frac,gamma", [(0.5, 4), (0.25, 1), (0.25, 5), (0.5, 2)])
+def test_tiny_selfspec_equals_greedy(torch, tiny_cfg, tiny_prompt, frac, gamma):
+    w = tiny_model_weights(tiny_cfg)
+    plan = oracle.layer_skip_plan(tiny_cfg.n_layers, frac)
+    m = make_model(tiny_cfg, w, draft_plan=plan)
+    greedy = m.greedy(tiny_prompt, 64)
+    reset(m)
+    out, acc = m.selfspec(tiny_prompt, 64, gamma)
+    assert out == greedy
+    assert all(0 <= k <= gamma for k in acc)
+
+
+@pytest.mark.parametrize("gamma", [3, 7])
+def test_tiny_full_plan_draft_accepts_all(torch, tiny_cfg, tiny_prompt, gamma):
+    w = tiny_model_weights(tiny_cfg)
+    m = make_model(tiny_cfg, w, draft_plan=list(range(tiny_cfg.n_layers)))
+    greedy = m.greedy(tiny_prompt, 40)
+    reset(m)
+    out, acc = m.selfspec(tiny_prompt, 40, gamma)
+    assert out == greedy
+    assert all(k == gamma for k in acc)
+
+
+def test_verify_rows_equal_decode_steps_bitwise(torch, tiny_cfg, tiny_prompt):
+    """Batch invariance: row j of a verify pass equals the one-token decode at
+    that position, bit for bit (fixed reduction orders; chunked attention on
+    absolute positions)."""
+    w = tiny_model_weights(tiny_cfg)
+    a = make_model(tiny_cfg, w)
+    b = make_model(tiny_cfg, w)
+    p = tiny_prompt
+    a.prefill(p[:70])
+    b.prefill(p[:70])
+    block = torch.tensor(p[70:86], dtype=torch.int32, device="cuda")
+    am, _, lg, _ = a.verify(block, logits=True)
+    for j in range(16):
+        amj, _, lgj, _ = b.verify(block[j:j + 1].clone(), logits=True)
+        assert torch.equal(lg[j], lgj[0]), j
+        assert int(am[j]) == int(amj[0])
+
+
+def test_rollback_equals_recompute_bitwise(torch, tiny_cfg, tiny_prompt):
+    w = tiny_model_weights(tiny_cfg)
+    a = make_model(tiny_cfg, w)
+    b = make_model(tiny_cfg, w)
+    p = tiny_prompt
+    a.prefill(p[:50])
+    a.verify(torch.tensor(p[50:58], dtype=torch.int32, device="cuda"))
+    a.rollback(0, 53)
+    b.prefill(p[:53])
+    blk = torch.tensor([11, 12, 13], dtype=torch.int32, device="cuda")
+    _, _, la, _ = a.verify(blk, logits=True)
+    _, _, lb, _ = b.verify(blk.clone(), logits=True)
+    assert torch.equal(la, lb)
+    assert a.kv_len(0) == 56
+
+
+def test_kv_cache_matches_oracle(torch, tiny_cfg, tiny_oracle, tiny_prompt):
+    w = tiny_model_weights(tiny_cfg)
+    m = make_model(tiny_cfg, w)
+    p = tiny_prompt[:77]
+    m.prefill(p)
+    oc = tiny_oracle.new_cache()
+    tiny_oracle.forward(oc, tiny_oracle.full_plan, p, 0, logits_from=None)
+    for layer in (0, tiny_cfg.n_layers - 1):
+        k, v = m.kv_export(0, layer, 77)
+        kr = oc.read(layer, 0, 77).reshape(77, tiny_cfg.n_kv_heads, tiny_cfg.head_dim)
+        vr = oc.read(layer, 1, 77).reshape(77, tiny_cfg.n_kv_heads, tiny_cfg.head_dim)
+        kg, vg = synth.bf16_to_f32(k), synth.bf16_to_f32(v)
+        assert np.allclose(kg, kr, atol=ATOL, rtol=RTOL)
+        assert np.allclose(vg, vr, atol=ATOL, rtol=RTOL)
+
+
+def test_kv_load_export_roundtrip(torch, tiny_cfg):
+    w = tiny_model_weights(tiny_cfg)
+    m = make_model(tiny_cfg, w)
+    k = synth.synthetic_kv(tiny_cfg, 2, 200, 0)
+    v = synth.synthetic_kv(tiny_cfg, 2, 200, 1)
+    m.kv_load(0, 2, k, v)
+    k2, v2 = m.kv_export(0, 2, 200)
+    assert np.array_equal(k, k2) and np.array_equal(v, v2)
+
+
+@pytest.mark.parametrize("ctx,n", [(0, 7), (63, 2), (64, 16), (130, 5), (255, 16)])
+def test_gqa_ragged_vocab_synthetic_context(torch, ctx, n):
+    """4 query heads per kv head, tied LM head, vocab 1000 (ragged last tile),
+    contexts loaded as synthetic KV that end inside / at page boundaries."""
+    cfg = small_gqa_cfg()
+    w = synth.make_weights(cfg)
+    m = make_model(cfg, w)
+    orc = oracle.Oracle(cfg, w)
+    oc = orc.new_cache()
+    for l in range(cfg.n_layers):
+        k = synth.synthetic_kv(cfg, l, max(ctx, 1), 0)[:ctx]
+        v = synth.synthetic_kv(cfg, l, max(ctx, 1), 1)[:ctx]
+        if ctx:
+            m.kv_load(0, l, k, v)
+            oc.load(l, k.reshape(ctx, -1), v.reshape(ctx, -1))
+    m.kv_set_len(0, ctx)
+    oc.set_len(ctx)
+    toks = synth.prompt(cfg, n, stream=ctx)
+    am, acc, lg, _ = m.verify(torch.tensor(toks, dtype=torch.int32, device="cuda"), logits=True)
+    ref, _, _ = orc.forward(oc, orc.full_plan, toks, ctx)
+    assert_logits_close(lg.cpu().numpy(), ref, "gqa ctx=%d n=%d" % (ctx, n))
+    argmax_mismatches(am.cpu().numpy(), ref)
+
+
+def test_moe_small_matches_oracle_and_modes_agree(torch):
+    import speculative_decoding_verify_pass_gb300 as sv
+    cfg = small_moe_cfg()
+    w = synth.make_weights(cfg)
+    m = make_model(cfg, w)
+    orc = oracle.Oracle(cfg, w)
+    p = synth.prompt(cfg, 40)
+    m.prefill(p[:30])
+    oc = orc.new_cache()
+    orc.forward(oc, orc.full_plan, p[:30], 0, logits_from=None)
+    results = {}
+    for mode in (sv.SPEC_MOE_PER_SLOT, sv.SPEC_MOE_DEDUP):
+        m.moe_mode(mode)
+        m.kv_set_len(0, 30)
+        am, acc, lg, ids = m.verify(torch.tensor(p[30:40], dtype=torch.int32, device="cuda"), logits=True,
+                                    expert_ids=True)
+        results[mode] = (am.cpu().numpy(), lg.cpu().numpy(), ids.cpu().numpy())
+    a, b = results[sv.SPEC_MOE_PER_SLOT], results[sv.SPEC_MOE_DEDUP]
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    gids = a[2]
+    ref, rids, _ = orc.forward(oc, orc.full_plan, p[30:40], 30, want_routing=True, forced_ids=np.maximum(gids, 0))
+    # the oracle's own (unforced) routing must pick the same experts
+    oc2 = orc.new_cache()
+    orc.forward(oc2, orc.full_plan, p[:30], 0, logits_from=None)
+    _, ids_free, _ = orc.forward(oc2, orc.full_plan, p[30:40], 30, want_routing=True)
+    assert np.array_equal(ids_free[1:], gids[1:])
+    assert np.all(gids[0] == -1)
+    assert_logits_close(a[1], ref, "moe")
+    argmax_mismatches(a[0], ref)
+
+
+def test_argument_errors(torch, tiny_cfg, tiny_model):
+    import speculative_decoding_verify_pass_gb300 as sv
+    m = tiny_model
+    reset(m)
+    with pytest.raises(sv.SpecError) as e:
+        m.verify(torch.zeros(17, dtype=torch.int32, device="cuda"))
+    assert e.value.status == sv.SPEC_ERR_INVALID_ARG
+    with pytest.raises(sv.SpecError) as e:
+        m.rollback(0, 5)
+    assert e.value.status == sv.SPEC_ERR_INVALID_ARG
+    with pytest.raises(sv.SpecError):
+        m.set_draft_plan([1, 2, 3])        # must keep layer 0
+    m.kv_set_len(0, tiny_cfg.max_ctx - 2)
+    with pytest.raises(sv.SpecError) as e:
+        m.verify(torch.zeros(4, dtype=torch.int32, device="cuda"))
+    assert e.value.status == sv.SPEC_ERR_CAPACITY
+    reset(m)
+    bad = torch.tensor([5, tiny_cfg.vocab + 3], dtype=torch.int32, device="cuda")
+    m.verify(bad)
+    with pytest.raises(sv.SpecError) as e:
+        m.check_error()
+    assert e.value.status == sv.SPEC_ERR_INVALID_ARG
+    m.check_error()

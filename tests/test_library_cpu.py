@@ -1,0 +1,87 @@
+"""CPU checks of the C ABI library and the host-side logic (no GPU needed).
+
+The library cross-compiles for sm_103a here and loads without a device;
+every symbol declared in include/spec.h must be exported.  No compute call is
+made."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+from oracle import closed_forms as cf
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "spec.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verify_pass_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary_calls():
+    names = declared_symbols()
+    for required in ("spec_model_create", "spec_prefill", "spec_draft_step", "spec_verify_step", "spec_kv_rollback",
+                     "spec_moe_mode", "spec_model_destroy", "spec_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_symbols() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_lists_every_declared_symbol():
+    import speculative_decoding_verify_pass_gb300 as sv
+    assert sorted(sv.EXPORTED) == declared_symbols()
+
+
+def test_argument_errors_need_no_device(lib):
+    """Host-side validation answers before any CUDA call."""
+    import speculative_decoding_verify_pass_gb300 as sv
+    L = sv.library()
+    assert L.spec_verify_step(None, None, 4, None, None, None, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_kv_rollback(None, 0, 3) == sv.SPEC_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    assert L.spec_model_create(None, None, None, 0, None, ctypes.byref(h)) == sv.SPEC_ERR_INVALID_ARG
+    assert b"null config" in L.spec_last_error()
+    bad = sv._config_c(synth.scaled(synth.tiny(), d_model=200))
+    assert L.spec_model_create(ctypes.byref(bad), None, None, 0, None, ctypes.byref(h)) == sv.SPEC_ERR_INVALID_ARG
+    assert b"multiple of 128" in L.spec_last_error()
+    bad = sv._config_c(synth.scaled(synth.tiny(), head_dim=96))
+    assert L.spec_model_create(ctypes.byref(bad), None, None, 0, None, ctypes.byref(h)) == sv.SPEC_ERR_INVALID_ARG
+
+
+def test_layer_skip_plan_matches_hand_worked_table():
+    import speculative_decoding_verify_pass_gb300 as sv
+    rows = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", "skip_sets.txt"))
+            if l.strip() and l[0] != "#"]
+    for L, f, a, b in rows:
+        keep = sv.layer_skip_plan(int(L), float(f))
+        assert [i for i in range(int(L)) if i not in keep] == list(range(int(a), int(b) + 1))
+
+
+def test_bench_byte_model_matches_closed_form():
+    import bench
+    for c in (synth.qwen3_4b(), synth.llama31_8b(), synth.qwen3_8b(), synth.tiny()):
+        for n, ctx in ((1, 0), (4, 2048), (16, 4096)):
+            assert bench.pass_bytes(c, n, ctx) == cf.pass_bytes(c, n, ctx).total
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The CUDA path and the binding must never reach the oracle."""
+    pkg = os.path.join(ROOT, "speculative_decoding_verify_pass_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower().replace("oracles", ""), f
