@@ -266,7 +266,9 @@ void set_mat(GemmParams& p, const PackedMat& m, const uint8_t* X, int epi, int g
     p.epi = epi;
     p.items_mode = 0;
     const long long I = (long long)m.T * m.KBs;
-    p.grid = (int)(I < grid_cap ? I : grid_cap);
+    // at most 64 CTAs may share one tile in the stream-K fixup
+    long long cap = grid_cap < 63ll * m.T ? grid_cap : 63ll * m.T;
+    p.grid = (int)(I < cap ? I : cap);
 }
 
 // Algorithmic bytes of one dense GEMM launch: weights once, the activation

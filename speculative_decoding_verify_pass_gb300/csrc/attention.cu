@@ -25,6 +25,7 @@ namespace sv {
 namespace {
 
 constexpr int kAttnThreads = 128;
+constexpr int kMaxChunks = 512;  // 65536 positions / 128
 
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const __grid_constant__ AttnParams p) {
@@ -175,6 +176,8 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const __grid
 // write the bf16 attention output into the O projection's operand.
 template <int HD>
 __global__ void __launch_bounds__(HD) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+    __shared__ float w_s[kMaxChunks];
+    __shared__ float l_s[kMaxChunks];
     const int qh = blockIdx.x, j = blockIdx.y, dim = threadIdx.x;
     pdl_launch_dependents();
     pdl_wait();
@@ -183,16 +186,34 @@ __global__ void __launch_bounds__(HD) attn_combine_kernel(const __grid_constant_
     const int total = p.st->len[p.which] + p.n;
     int nc = (total + kAttnChunk - 1) / kAttnChunk;
     if (nc > p.nch) nc = p.nch;
-    float M = -1e30f;
-    for (int c = 0; c < nc; ++c) M = fmaxf(M, p.part_ml[(size_t)(h * p.nch + c) * 64 + r].x);
-    float L = 0.f, O = 0.f;
-    for (int c = 0; c < nc; ++c) {
-        const size_t slot = (size_t)(h * p.nch + c) * 64 + r;
-        const float2 ml = p.part_ml[slot];
-        const float w = exp2f(ml.x - M);
-        L += w * ml.y;
-        O += w * p.part_o[slot * HD + dim];
+    if (nc > kMaxChunks) nc = kMaxChunks;
+    // all chunk statistics in parallel, then the merge weights
+    for (int c = dim; c < nc; c += HD) {
+        const float2 ml = p.part_ml[(size_t)(h * p.nch + c) * 64 + r];
+        w_s[c] = ml.x;
+        l_s[c] = ml.y;
     }
+    __syncthreads();
+    float M = -1e30f;
+    for (int c = 0; c < nc; ++c) M = fmaxf(M, w_s[c]);
+    float L = 0.f;
+    for (int c = 0; c < nc; ++c) L += exp2f(w_s[c] - M) * l_s[c];
+    __syncthreads();
+    for (int c = dim; c < nc; c += HD) w_s[c] = exp2f(w_s[c] - M);
+    __syncthreads();
+    // unnormalised outputs: independent loads, summed in chunk order
+    const float* po = p.part_o + ((size_t)h * p.nch * 64 + r) * HD + dim;
+    const size_t cstride = (size_t)64 * HD;
+    float O = 0.f;
+    int c = 0;
+    for (; c + 8 <= nc; c += 8) {
+        float v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = po[(size_t)(c + u) * cstride];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) O += w_s[c + u] * v[u];
+    }
+    for (; c < nc; ++c) O += w_s[c] * po[(size_t)c * cstride];
     const int k = qh * HD + dim;
     *reinterpret_cast<uint16_t*>(p.xf_out + (size_t)(k >> 6) * kStageXBytes + xfrag_offset(j, k & 63)) = f2bf(O / L);
 }

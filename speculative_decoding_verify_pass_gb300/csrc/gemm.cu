@@ -14,7 +14,9 @@
 //    fragment with one 16-byte shared load.
 //  * The activation operand (n x 64 per stage, <= 2 KB) is kept by the
 //    producing kernel in B-fragment order and bulk-copied next to the weights.
-//  * An 8-deep ring of stages keeps 144 KB per SM in flight.
+//  * An 8-deep ring of stages keeps 128 KB of weights in flight per SM.  The
+//    CTA takes over half of the SM's shared memory on purpose: a persistent
+//    grid with a static split must not have two of its CTAs on one SM.
 //  * Work split: stream-K over the flattened (tile, k-block) space, each CTA
 //    one contiguous range; a tile split between CTAs is summed by the last CTA
 //    to arrive, in fixed contributor order (deterministic, and independent of
@@ -34,13 +36,14 @@ namespace sv {
 
 namespace {
 
-constexpr int kStages = 8;
+constexpr int kStages = 8;  // 128 KB of weights in flight per SM
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
 constexpr int kCsLd = 20;  // padded row stride of the fp32 tile
 constexpr int kMaxItems = kMaxBlock * kMaxTopK;
 constexpr int kPartFloats = kTileRows * kMaxBlock;
+constexpr int kMaxContrib = 64;  // CTAs that can share one tile (checked on the host)
 
 struct Item {
     int expert;
@@ -55,6 +58,7 @@ struct __align__(128) GemmSmem {
     uint64_t full[kStages];
     uint64_t empty[kStages];
     float rstd[kMaxBlock];
+    int slots[kMaxContrib];
     int flag;
     int n_items;
     Item items[kMaxItems];
@@ -461,13 +465,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         named_bar_sync(1, kConsumers);
 
         if (!p.items_mode && !(b0 == 0 && b1 == p.KBs)) {
-            // split tile: publish the partial, the last contributor reduces
+            // split tile: publish the partial; the last contributor to arrive
+            // sums all partials in contributor order
             const int cf = sk_owner((long long)tile * p.KBs, I, p.grid);
             const int cl = sk_owner((long long)tile * p.KBs + p.KBs - 1, I, p.grid);
+            const int ncontrib = cl - cf + 1;
             const int me = blockIdx.x;
             const int myslot = 2 * me + ((sk_start(me, I, p.grid) / p.KBs == tile) ? 0 : 1);
-            float* dst = p.partials + (size_t)myslot * kPartFloats;
-            for (int e = tid; e < kPartFloats; e += kConsumers) dst[e] = cs[(e >> 4) * kCsLd + (e & 15)];
+            // thread tid owns partial elements [tid*8, tid*8+8): row tid/2, cols (tid&1)*8..+7
+            const float* crow = cs + (tid >> 1) * kCsLd + (tid & 1) * 8;
+            float4* dst = reinterpret_cast<float4*>(p.partials + (size_t)myslot * kPartFloats) + tid * 2;
+            __stcg(dst, make_float4(crow[0], crow[1], crow[2], crow[3]));
+            __stcg(dst + 1, make_float4(crow[4], crow[5], crow[6], crow[7]));
+            if (tid < ncontrib && tid < kMaxContrib) {
+                const int cc = cf + tid;
+                sm.slots[tid] = 2 * cc + ((sk_start(cc, I, p.grid) / p.KBs == tile) ? 0 : 1);
+            }
             __threadfence();
             named_bar_sync(1, kConsumers);
             if (tid == 0) {
@@ -477,14 +490,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             named_bar_sync(1, kConsumers);
             if (!sm.flag) continue;
             __threadfence();
-            for (int e = tid; e < kPartFloats; e += kConsumers) {
-                float v = 0.f;
-                for (int cc = cf; cc <= cl; ++cc) {
-                    const int sl = 2 * cc + ((sk_start(cc, I, p.grid) / p.KBs == tile) ? 0 : 1);
-                    v += __ldcg(p.partials + (size_t)sl * kPartFloats + e);
+            float4 s0 = make_float4(0.f, 0.f, 0.f, 0.f), s1 = s0;
+            for (int base = 0; base < ncontrib; base += 4) {
+                float4 v[4][2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (base + u < ncontrib) {
+                        const int sl = (base + u < kMaxContrib) ? sm.slots[base + u] : 0;
+                        const float4* src = reinterpret_cast<const float4*>(p.partials + (size_t)sl * kPartFloats) + tid * 2;
+                        v[u][0] = __ldcg(src);
+                        v[u][1] = __ldcg(src + 1);
+                    }
                 }
-                cs[(e >> 4) * kCsLd + (e & 15)] = v;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (base + u < ncontrib) {
+                        s0.x += v[u][0].x; s0.y += v[u][0].y; s0.z += v[u][0].z; s0.w += v[u][0].w;
+                        s1.x += v[u][1].x; s1.y += v[u][1].y; s1.z += v[u][1].z; s1.w += v[u][1].w;
+                    }
+                }
             }
+            float* wrow = cs + (tid >> 1) * kCsLd + (tid & 1) * 8;
+            wrow[0] = s0.x; wrow[1] = s0.y; wrow[2] = s0.z; wrow[3] = s0.w;
+            wrow[4] = s1.x; wrow[5] = s1.y; wrow[6] = s1.z; wrow[7] = s1.w;
             if (tid == 0) p.counters[tile] = 0;
             named_bar_sync(1, kConsumers);
         }

@@ -104,7 +104,23 @@ __global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ Acc
     if (warp < p.n) {
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        for (int t = lane; t < p.T; t += 32) {
+        int t = lane;
+        for (; t + 7 * 32 < p.T; t += 8 * 32) {  // eight independent loads in flight per lane
+            float v[8];
+            int ix[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                v[u] = p.amax_val[warp * p.T + t + u * 32];
+                ix[u] = p.amax_idx[warp * p.T + t + u * 32];
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (v[u] > best || (v[u] == best && ix[u] < bi)) {
+                    best = v[u];
+                    bi = ix[u];
+                }
+        }
+        for (; t < p.T; t += 32) {
             const float v = p.amax_val[warp * p.T + t];
             const int i = p.amax_idx[warp * p.T + t];
             if (v > best || (v == best && i < bi)) {
