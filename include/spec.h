@@ -231,6 +231,29 @@ spec_status spec_profile_enable(spec_handle h, int32_t enable);
  * once) and the launch count.  Resets the record. */
 spec_status spec_profile_read(spec_handle h, double* total_ms, double* total_bytes, int32_t* launches);
 
+/* Greedy accept from caller-computed logits, without any device allocation.
+ * The pages have no counterpart to this call.  It serves callers that cannot
+ * allocate device memory where they need the accept decision: a process
+ * whose memory pool already owns the device, a serving loop that forbids
+ * allocation after warm-up, or a thread that must not stall the device with
+ * cudaMalloc.  It computes what the accept step of spec_verify_step computes:
+ * d_argmax[j] = argmax of row j of d_logits ([n][vocab] float32, lowest id on
+ * ties) and d_accept_len[0] = number of leading j < n-1 with
+ * d_block[j+1] == d_argmax[j]; the caller passes and owns all five buffers.
+ * Limits: 1 <= n <= 16 and 1 <= vocab <= 2,097,152; other sizes, or a null
+ * pointer, return SPEC_ERR_INVALID_ARG and enqueue nothing.
+ * Scratch: a fixed 128 KB array inside the library, which every GPU that
+ * loads the library holds until the process exits; no cudaMalloc, cudaFree or
+ * allocating library routine is called.  The first call on a device looks up
+ * that array's device address with the device current, so make the first call
+ * on each device before any stream capture.  All calls on a device share the
+ * array: calls whose kernels can overlap on the GPU (different streams with
+ * no ordering between them) race; calls on one stream are ordered and safe.
+ * Each call overwrites every scratch entry it reads, so nothing has to start
+ * at zero.  Asynchronous on cuda_stream (a cudaStream_t, NULL = default). */
+spec_status spec_accept_from_logits_noalloc(const float* d_logits, int32_t n, int32_t vocab, const int32_t* d_block,
+                                            int32_t* d_argmax, int32_t* d_accept_len, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -25,7 +25,8 @@ SPEC_MAX_BLOCK = 16
 EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "spec_set_stream", "spec_prefill",
             "spec_draft_step", "spec_verify_step", "spec_kv_rollback", "spec_moe_mode", "spec_last_error",
             "spec_check_error", "spec_kv_len", "spec_kv_load", "spec_kv_export", "spec_kv_set_len",
-            "spec_moe_force_routing", "spec_last_launch_count", "spec_profile_enable", "spec_profile_read"]
+            "spec_moe_force_routing", "spec_last_launch_count", "spec_profile_enable", "spec_profile_read",
+            "spec_accept_from_logits_noalloc"]
 
 
 class SpecError(RuntimeError):
@@ -89,6 +90,7 @@ def library():
         "spec_profile_enable": [vp, i32],
         "spec_profile_read": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                               ctypes.POINTER(i32)],
+        "spec_accept_from_logits_noalloc": [vp, i32, i32, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -182,6 +184,15 @@ def spec_profile_read(h):
     ms, by, n = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_int32(0)
     _check(library().spec_profile_read(h, ctypes.byref(ms), ctypes.byref(by), ctypes.byref(n)))
     return float(ms.value), float(by.value), int(n.value)
+
+
+def spec_accept_from_logits_noalloc(d_logits, d_block, d_argmax, d_accept_len, stream=None):
+    """Argmax rows and accept_len from caller-computed logits [n][vocab]; the
+    library allocates nothing for this call (fixed in-library scratch)."""
+    n, vocab = int(d_logits.shape[0]), int(d_logits.shape[1])
+    st = _stream() if stream is None else ctypes.c_void_p(stream)
+    _check(library().spec_accept_from_logits_noalloc(_ptr(d_logits), n, vocab, _ptr(d_block), _ptr(d_argmax),
+                                                     _ptr(d_accept_len), st))
 
 
 # ----------------------------------------------------------------------------

@@ -106,6 +106,11 @@ struct spec_model {
 };
 
 namespace {
+}  // namespace
+
+void sv::set_last_error(const char* msg) { g_err = msg ? msg : ""; }
+
+namespace {
 
 spec_status dalloc(spec_model* h, void** p, size_t bytes, std::vector<void*>* owner = nullptr) {
     if (bytes == 0) bytes = 16;

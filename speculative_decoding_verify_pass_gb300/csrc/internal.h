@@ -157,4 +157,7 @@ cudaError_t launch_pack(const PackSrc& s, const PackedMat& m, cudaStream_t st);
 cudaError_t launch_kv_io(uint16_t* pool, const int* block_table, uint16_t* logical, int ctx, int hkv, int hd,
                          bool to_pool, cudaStream_t s);
 
+// Sets the thread-local message returned by spec_last_error (api.cu).
+void set_last_error(const char* msg);
+
 }  // namespace sv
