@@ -71,7 +71,7 @@ enum { SPEC_CACHE_TARGET = 0, SPEC_CACHE_DRAFT = 1 };
  * l >= first_moe_layer use a softmax router over n_experts, top_k routed
  * SwiGLU experts of width expert_ffn and n_shared_experts shared experts of
  * the same width; earlier layers use a dense SwiGLU FFN of width ffn_dim.
- * Shape rules (checked): d_model is a multiple of 128; n_heads*head_dim,
+ * Shape rules (checked): d_model is a multiple of 128 up to 8192; n_heads*head_dim,
  * ffn_dim and expert_ffn are multiples of 64; head_dim is 64 or 128; n_heads is a multiple of
  * n_kv_heads with at most 4 query heads per kv head; n_experts <= 64;
  * top_k <= 8; 1 <= max_ctx <= 65536. */
@@ -230,6 +230,16 @@ spec_status spec_profile_enable(spec_handle h, int32_t enable);
  * summed algorithmic bytes (weights + activation operand + outputs, each
  * once) and the launch count.  Resets the record. */
 spec_status spec_profile_read(spec_handle h, double* total_ms, double* total_bytes, int32_t* launches);
+
+/* Benchmark hook: while enabled, each persistent pass kernel records, per CTA
+ * and phase, four global-timer stamps (phase entered, grid barrier passed,
+ * phase work done, last streamed stage consumed or 0).  Allocates the trace
+ * buffer on enable; synchronous. */
+spec_status spec_trace_enable(spec_handle h, int32_t enable);
+
+/* Copy the last traced pass's stamps ([nctas][nphase][4] nanoseconds) to the
+ * host array out (capacity entries).  Synchronises the stream. */
+spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int32_t* nphase, int32_t* nctas);
 
 /* Greedy accept from caller-computed logits, without any device allocation.
  * The pages have no counterpart to this call.  It serves callers that cannot

@@ -13,6 +13,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <string>
 #include <vector>
 
@@ -95,6 +96,17 @@ struct spec_model {
     int host_len[2] = {0, 0};   // upper bounds of the device lengths
     bool len_exact[2] = {true, true};
     int launches = 0;
+    bool use_pass = false;              // persistent pass kernel for dense models (SPEC_PASS_KERNEL=1)
+    int* gbar = nullptr;                // pass kernel's grid-barrier counters
+    long long* trace = nullptr;         // phase timestamps of the last traced pass
+    size_t trace_cap = 0;
+    int trace_nphase = 0;
+    struct PassTable {
+        PhaseDesc* dev;
+        int count;
+        double gemm_bytes;   // algorithmic bytes of the table's GEMM phases
+    };
+    std::map<int, PassTable> tables;   // (which, n, lm) -> device phase list
     bool profiling = false;
     struct ProfRec {
         cudaEvent_t a, b;
@@ -170,7 +182,8 @@ spec_status copy_vec(spec_model* h, uint16_t** dst, const void* src, size_t coun
 
 spec_status validate_config(const spec_model_config* c) {
     if (!c) return fail(SPEC_ERR_INVALID_ARG, "null config");
-    if (c->n_layers < 1 || c->d_model < 128 || c->d_model % 128) return fail(SPEC_ERR_INVALID_ARG, "d_model must be a positive multiple of 128");
+    if (c->n_layers < 1 || c->d_model < 128 || c->d_model % 128 || c->d_model > 8192)
+        return fail(SPEC_ERR_INVALID_ARG, "d_model must be a multiple of 128 in 128..8192");
     if (c->head_dim != 64 && c->head_dim != 128) return fail(SPEC_ERR_INVALID_ARG, "head_dim must be 64 or 128");
     if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads || c->n_heads / c->n_kv_heads > 4)
         return fail(SPEC_ERR_INVALID_ARG, "n_heads must be a multiple of n_kv_heads with at most 4 per kv head");
@@ -271,8 +284,8 @@ void set_mat(GemmParams& p, const PackedMat& m, const uint8_t* X, int epi, int g
     p.epi = epi;
     p.items_mode = 0;
     const long long I = (long long)m.T * m.KBs;
-    // at most 64 CTAs may share one tile in the stream-K fixup
-    long long cap = grid_cap < 63ll * m.T ? grid_cap : 63ll * m.T;
+    // at most 160 CTAs may share one tile in the stream-K fixup
+    long long cap = grid_cap < 159ll * m.T ? grid_cap : 159ll * m.T;
     p.grid = (int)(I < cap ? I : cap);
 }
 
@@ -312,10 +325,16 @@ spec_status gemm(spec_model* h, const GemmParams& p) {
 }
 
 // One pass of n tokens through a plan (target: all layers; draft: kept layers).
+spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
+                            int32_t* d_accept, float* d_logits, int32_t* d_pair, int32_t* d_token,
+                            const int32_t* d_block);
+
 spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
                      int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair, int32_t* d_token,
                      const int32_t* d_block) {
     const spec_model_config& c = h->c;
+    if (h->use_pass && c.n_experts == 0)
+        return run_pass_kernel(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_pair, d_token, d_block);
     const std::vector<int>& plan = which == 0 ? h->plan_full : h->plan_draft;
     const int d = c.d_model, hd = c.head_dim;
     const int G = h->num_sms;
@@ -487,7 +506,169 @@ spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, P
     return SPEC_OK;
 }
 
+// ---- persistent pass kernel (dense models) ----
+AttnParams attn_params(spec_model* h, int which, int n, uint16_t* kpool, uint16_t* vpool) {
+    AttnParams a{};
+    a.qbuf = h->qbuf;
+    a.kpool = kpool;
+    a.vpool = vpool;
+    a.block_table = h->block_table;
+    a.part_o = h->attn_o;
+    a.part_ml = h->attn_ml;
+    a.xf_out = h->xf_o;
+    a.st = h->st;
+    a.which = which;
+    a.n = n;
+    a.n_heads = h->c.n_heads;
+    a.n_kv_heads = h->c.n_kv_heads;
+    a.head_dim = h->c.head_dim;
+    a.nch = h->nch;
+    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->c.head_dim));
+    return a;
+}
+
+spec_status pass_table(spec_model* h, int which, int n, bool lm, spec_model::PassTable* out) {
+    const int key = which * 10000 + n * 10 + (lm ? 1 : 0);
+    auto f = h->tables.find(key);
+    if (f != h->tables.end()) {
+        *out = f->second;
+        return SPEC_OK;
+    }
+    const spec_model_config& c = h->c;
+    const std::vector<int>& plan = which == 0 ? h->plan_full : h->plan_draft;
+    const int d = c.d_model, G = h->num_sms;
+    std::vector<PhaseDesc> v;
+    auto phase = [&](int kind) -> PhaseDesc& {
+        v.emplace_back();
+        std::memset(&v.back(), 0, sizeof(PhaseDesc));
+        v.back().kind = kind;
+        return v.back();
+    };
+    {
+        PhaseDesc& e = phase(PH_EMBED);
+        e.e.embed = h->embed;
+        e.e.n = n;
+        e.e.d = d;
+        e.e.vocab = c.vocab;
+        e.e.x = h->x;
+        e.e.g_next = h->L[plan[0]].attn_norm;
+        e.e.xf_out = h->xf_norm;
+        e.e.ss_out = h->ss;
+        e.e.st = h->st;
+    }
+    for (size_t si = 0; si < plan.size(); ++si) {
+        const int l = plan[si];
+        LayerW& W = h->L[l];
+        const uint16_t* g_after = (si + 1 < plan.size()) ? h->L[plan[si + 1]].attn_norm : h->final_norm;
+        uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
+        uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
+        GemmParams p = base_params(h, which, n);
+        set_mat(p, W.qkv, h->xf_norm, EPI_QKV, G);
+        p.norm_dim = d;
+        p.rope = h->rope;
+        p.qbuf = h->qbuf;
+        p.kpool = kpool;
+        p.vpool = vpool;
+        p.block_table = h->block_table;
+        phase(PH_GEMM).g = p;
+        phase(PH_ATTN).a = attn_params(h, which, n, kpool, vpool);
+        phase(PH_COMB).a = attn_params(h, which, n, kpool, vpool);
+        p = base_params(h, which, n);
+        set_mat(p, W.o, h->xf_o, EPI_RESID, G);
+        p.g_next = W.ffn_norm;
+        p.xf_out = h->xf_norm;
+        phase(PH_GEMM).g = p;
+        p = base_params(h, which, n);
+        set_mat(p, W.gu, h->xf_norm, EPI_SWIGLU, G);
+        p.norm_dim = d;
+        p.xf_out = h->xf_down;
+        phase(PH_GEMM).g = p;
+        p = base_params(h, which, n);
+        set_mat(p, W.down, h->xf_down, EPI_RESID, G);
+        p.g_next = g_after;
+        p.xf_out = h->xf_norm;
+        phase(PH_GEMM).g = p;
+    }
+    if (lm) {
+        GemmParams p = base_params(h, which, n);
+        set_mat(p, h->lm, h->xf_norm, EPI_LMHEAD, G);
+        p.norm_dim = d;
+        p.amax_val = h->amax_val;
+        p.amax_idx = h->amax_idx;
+        phase(PH_GEMM).g = p;
+        phase(PH_ACCEPT);
+    } else {
+        phase(PH_ADVANCE);
+    }
+    PhaseDesc* dev = nullptr;
+    spec_status s = dalloc(h, reinterpret_cast<void**>(&dev), sizeof(PhaseDesc) * v.size());
+    if (s != SPEC_OK) return s;
+    CU(cudaMemcpyAsync(dev, v.data(), sizeof(PhaseDesc) * v.size(), cudaMemcpyHostToDevice, h->stream));
+    CU(cudaStreamSynchronize(h->stream));
+    double gb = 0.0;
+    for (const PhaseDesc& ph : v)
+        if (ph.kind == PH_GEMM) gb += gemm_bytes(ph.g);
+    h->tables[key] = {dev, (int)v.size(), gb};
+    *out = h->tables[key];
+    return SPEC_OK;
+}
+
+spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
+                            int32_t* d_accept, float* d_logits, int32_t* d_pair, int32_t* d_token,
+                            const int32_t* d_block) {
+    const bool lm = mode != PASS_PREFILL_MID;
+    spec_model::PassTable tab{};
+    spec_status s = pass_table(h, which, n, lm, &tab);
+    if (s != SPEC_OK) return s;
+    PassParams P{};
+    P.phases = tab.dev;
+    P.nphase = tab.count;
+    P.n = n;
+    P.which = which;
+    P.mode = mode == PASS_VERIFY ? ACC_VERIFY : (mode == PASS_DRAFT ? ACC_DRAFT : ACC_PREFILL);
+    P.nch = h->nch;
+    P.st = h->st;
+    P.gbar = h->gbar;
+    P.tokens = d_tokens;
+    P.logits = d_logits;
+    P.block = d_block;
+    P.out_argmax = d_argmax;
+    P.out_accept = d_accept;
+    P.out_pair = d_pair;
+    P.out_token = d_token;
+    P.amax_val = h->amax_val;
+    P.amax_idx = h->amax_idx;
+    P.lm_T = h->lm.T;
+    if (h->trace) {
+        const size_t need = (size_t)h->num_sms * tab.count * 4;
+        if (need <= h->trace_cap) {
+            P.trace = h->trace;
+            h->trace_nphase = tab.count;
+        }
+    }
+    spec_model::ProfRec r{};
+    if (h->profiling) {
+        // exact context for the KV bytes (profiling only: synchronises)
+        if ((s = sync_lengths(h)) != SPEC_OK) return s;
+        const size_t layers = which == 0 ? h->plan_full.size() : h->plan_draft.size();
+        const double kv = (double)layers * 2.0 * h->c.n_kv_heads * h->c.head_dim * 2.0 * (h->host_len[which] + n);
+        r.bytes = tab.gemm_bytes + kv + (double)n * h->c.d_model * 2.0;
+        CU(cudaEventCreate(&r.a));
+        CU(cudaEventCreate(&r.b));
+        CU(cudaEventRecord(r.a, h->stream));
+    }
+    CU(launch_pass(P, h->num_sms, h->stream));
+    ++h->launches;
+    if (h->profiling) {
+        CU(cudaEventRecord(r.b, h->stream));
+        h->prof.push_back(r);
+    }
+    return SPEC_OK;
+}
+
 void free_all(spec_model* h) {
+    if (h->trace) cudaFree(h->trace);
+    h->trace = nullptr;
     for (void* p : h->draft_allocs) cudaFree(p);
     for (void* p : h->allocs) cudaFree(p);
     h->allocs.clear();
@@ -559,7 +740,9 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     }
     h->num_sms = prop.multiProcessorCount;
     if (const char* e = std::getenv("SPEC_NO_PDL")) h->pdl = !(e[0] == '1');
+    if (const char* e = std::getenv("SPEC_PASS_KERNEL")) h->use_pass = (e[0] == '1');
     TRYCU(gemm_configure(h->device));
+    TRYCU(pass_configure(h->device));
     TRYCU(attention_configure(h->device));
 
     const int d = c.d_model, hd = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads;
@@ -672,8 +855,9 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     TRY(dalloc_t(h, &h->xf_down, (size_t)(ffn_max / kKBlock) * kStageXBytes));
     TRY(dalloc_t(h, &h->qbuf, (size_t)kMaxBlock * qw));
     TRY(dalloc_t(h, &h->ss, (size_t)kMaxBlock * (d / kTileRows)));
-    TRY(dalloc_t(h, &h->attn_o, (size_t)Hkv * h->nch * 64 * hd));
-    TRY(dalloc_t(h, &h->attn_ml, (size_t)Hkv * h->nch * 64));
+    TRY(dalloc_t(h, &h->attn_o, (size_t)Hkv * 2 * h->nch * 64 * hd));
+    TRY(dalloc_t(h, &h->attn_ml, (size_t)Hkv * 2 * h->nch * 64));
+    TRY(dalloc_t(h, &h->gbar, 2));
     TRY(dalloc_t(h, &h->gpart, (size_t)2 * h->num_sms * kTileRows * kMaxBlock));
     TRY(dalloc_t(h, &h->gcnt, (size_t)h->max_T + 1));
     TRY(dalloc_t(h, &h->amax_val, (size_t)kMaxBlock * h->lm.T));
@@ -818,6 +1002,7 @@ spec_status spec_check_error(spec_handle h) {
         int zero = 0;
         CU(cudaMemcpy(&h->st->error, &zero, sizeof(int), cudaMemcpyHostToDevice));
         CU(cudaMemset(h->gcnt, 0, sizeof(int) * (h->max_T + 1)));
+        CU(cudaMemset(h->gbar, 0, sizeof(int) * 2));
         return fail(err == 10 ? SPEC_ERR_INVALID_ARG : SPEC_ERR_TIMEOUT,
                     err == 10 ? "a token id outside [0, vocab) was replaced by 0" : "device error code %d", err);
     }
@@ -894,6 +1079,32 @@ int32_t spec_last_launch_count(spec_handle h) { return h ? h->launches : -1; }
 spec_status spec_profile_enable(spec_handle h, int32_t enable) {
     if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
     h->profiling = enable != 0;
+    return SPEC_OK;
+}
+
+spec_status spec_trace_enable(spec_handle h, int32_t enable) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    CU(cudaStreamSynchronize(h->stream));
+    if (enable && !h->trace) {
+        h->trace_cap = (size_t)h->num_sms * 4096 * 4;
+        CU(cudaMalloc(&h->trace, h->trace_cap * sizeof(long long)));
+    } else if (!enable && h->trace) {
+        cudaFree(h->trace);
+        h->trace = nullptr;
+        h->trace_cap = 0;
+    }
+    return SPEC_OK;
+}
+
+spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int32_t* nphase, int32_t* nctas) {
+    if (!h || !out || !nphase || !nctas) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (!h->trace || h->trace_nphase == 0) return fail(SPEC_ERR_STATE, "no traced pass");
+    const size_t count = (size_t)h->num_sms * h->trace_nphase * 4;
+    if ((size_t)capacity < count) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", count);
+    CU(cudaStreamSynchronize(h->stream));
+    CU(cudaMemcpy(out, h->trace, count * sizeof(long long), cudaMemcpyDeviceToHost));
+    *nphase = h->trace_nphase;
+    *nctas = h->num_sms;
     return SPEC_OK;
 }
 

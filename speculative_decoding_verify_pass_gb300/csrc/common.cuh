@@ -104,6 +104,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     for (uint32_t i = 0; i < (1u << 24); ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i > 64) __nanosleep(i < 4096 ? 32 : 256);
+        // once any wait of the launch has given up, stop waiting at all
+        if ((i & 1023) == 1023 && err && *reinterpret_cast<volatile int*>(err) != 0) return false;
     }
     if (err) atomicCAS(err, 0, site);
     return false;
@@ -117,6 +119,24 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint3
             smem_u32(smem_dst)),
         "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Release-ordered reduction at GPU scope (no return value, no round trip):
+// every write the CTA made before the preceding CTA barrier is visible to a
+// thread that acquires the counter afterwards.
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu_i32(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bulk prefetch of a global range into L2 (no shared-memory destination, no
+// completion): warms the 129 MB L2 ahead of the TMA loads that will read it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
 
 // Programmatic dependent launch: let the next kernel start its prologue, and

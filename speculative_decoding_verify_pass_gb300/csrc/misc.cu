@@ -78,14 +78,36 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant_
     if (j < p.n) {
         const int R0 = tile * kTileRows + rg * 8;
         float* xr = p.x + (size_t)j * p.d + R0;
+        // all slot rows at once (independent loads), then the sum in slot order
+        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float4 ys[kMaxTopK][2];
+        float gs[kMaxTopK];
+#pragma unroll
+        for (int s = 0; s < kMaxTopK; ++s) {
+            if (s < p.top_k) {
+                const float* src = p.y_slot + ((size_t)j * p.top_k + s) * p.d + R0;
+                ys[s][0] = *reinterpret_cast<const float4*>(src);
+                ys[s][1] = *reinterpret_cast<const float4*>(src + 4);
+                gs[s] = p.gates[j * p.top_k + s];
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < kMaxTopK; ++s) {
+            if (s < p.top_k) {
+                const float a[8] = {ys[s][0].x, ys[s][0].y, ys[s][0].z, ys[s][0].w,
+                                    ys[s][1].x, ys[s][1].y, ys[s][1].z, ys[s][1].w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] += gs[s] * a[e];
+            }
+        }
+        const float4 x0 = *reinterpret_cast<const float4*>(xr), x1 = *reinterpret_cast<const float4*>(xr + 4);
+        const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         float v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float y = 0.f;
-            for (int s = 0; s < p.top_k; ++s)
-                y += p.gates[j * p.top_k + s] * p.y_slot[((size_t)j * p.top_k + s) * p.d + R0 + e];
-            if (p.y_shared) y += p.y_shared[(size_t)j * p.d + R0 + e];
-            v[e] = xr[e] + y;
+            float t = y[e];
+            if (p.y_shared) t += p.y_shared[(size_t)j * p.d + R0 + e];
+            v[e] = xv[e] + t;
         }
         ssum = store_residual8(xr, v, j, R0, p.g_next, p.xf_out);
     }

@@ -244,3 +244,29 @@ def test_argument_errors(torch, tiny_cfg, tiny_model):
         m.check_error()
     assert e.value.status == sv.SPEC_ERR_INVALID_ARG
     m.check_error()
+
+
+@pytest.mark.parametrize("use_pass", ["0", "1"])
+def test_both_launch_paths_match_oracle(torch, tiny_cfg, tiny_oracle, tiny_prompt, monkeypatch, use_pass):
+    """Dense models run either as one persistent pass kernel (default) or as
+    one launch per phase; both must match the oracle and the golden greedy."""
+    monkeypatch.setenv("SPEC_PASS_KERNEL", use_pass)
+    w = tiny_model_weights(tiny_cfg)
+    m = make_model(tiny_cfg, w, draft_plan=oracle.layer_skip_plan(tiny_cfg.n_layers, 0.5))
+    orc = tiny_oracle
+    p = tiny_prompt
+    m.prefill(p[:90])
+    oc = orc.new_cache()
+    orc.forward(oc, orc.full_plan, p[:90], 0, logits_from=None)
+    for n in (1, 7, 16):
+        am, acc, lg, _ = m.verify(torch.tensor(p[90:90 + n], dtype=torch.int32, device="cuda"), logits=True)
+        ref, _, _ = orc.forward(oc, orc.full_plan, p[90:90 + n], 90)
+        assert_logits_close(lg.cpu().numpy(), ref, "path %s n=%d" % (use_pass, n))
+        argmax_mismatches(am.cpu().numpy(), ref)
+        m.rollback(0, 90)
+        oc.truncate(90)
+    m.check_error()
+    want = [int(t) for t in open(os.path.join(GOLDEN, "tiny_greedy.txt")).read().split("\n")[-2].split()]
+    m2 = make_model(tiny_cfg, w)
+    assert m2.greedy(p, 64) == want
+    m2.check_error()
