@@ -46,14 +46,8 @@ def measured_peaks():
 
 
 def pass_bytes(cfg, n, ctx, plan=None):
-    """Algorithmic bytes of one dense pass: executed layers' weights, LM head,
-    KV read over ctx, KV rows written, embedding rows."""
-    plan = list(range(cfg.n_layers)) if plan is None else plan
-    d, hd = cfg.d_model, cfg.head_dim
-    qw, kw = cfg.n_heads * hd, cfg.n_kv_heads * hd
-    per_layer = ((qw + 2 * kw) * d + d * qw + 3 * cfg.ffn_dim * d) * 2
-    kv = 2 * kw * 2
-    return len(plan) * (per_layer + kv * (ctx + n)) + cfg.vocab * d * 2 + n * d * 2
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    return stepmodel.pass_bytes(cfg, n, ctx, plan)
 
 
 # ----------------------------------------------------------------------------
@@ -427,6 +421,267 @@ def run_reference(args):
         "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
 
 
+# ----------------------------------------------------------------------------
+# measurement suites (one JSON line per point; not the default bench line)
+# ----------------------------------------------------------------------------
+def _emit(d):
+    print(json.dumps(d), flush=True)
+
+
+def _model_at_context(cfg, ctx, draft_plan=None):
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    w = synth.make_weights(cfg)
+    m = sv.Model(cfg, w, draft_plan=draft_plan)
+    plan = draft_plan or []
+    for l in range(cfg.n_layers):
+        k = synth.synthetic_kv(cfg, l, ctx, 0)
+        v = synth.synthetic_kv(cfg, l, ctx, 1)
+        m.kv_load(0, l, k, v)
+        if l in plan:
+            m.kv_load(1, plan.index(l), k, v)
+    m.kv_set_len(0, ctx)
+    if plan:
+        m.kv_set_len(1, ctx)
+    return m, w
+
+
+def _time_calls(torch, fn, reps=10, warm=3):
+    for _ in range(warm):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps  # us
+
+
+def _verify_us(torch, sv, m, toks, ctx, reps=10):
+    n = len(toks)
+    blk = torch.tensor(toks, dtype=torch.int32, device="cuda")
+    am = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def one():
+        sv.spec_verify_step(m.h, blk, am, ac)
+        sv.spec_kv_rollback(m.h, 0, ctx)
+    return _time_calls(torch, one, reps)
+
+
+def _draft_us(torch, sv, m, ctx, reps=10):
+    t = torch.tensor([1], dtype=torch.int32, device="cuda")
+    out = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def one():
+        sv.spec_draft_step(m.h, t, out)
+        sv.spec_kv_rollback(m.h, 1, ctx)
+    return _time_calls(torch, one, reps)
+
+
+def suite_sweep(args):
+    """Verify time / HBM bandwidth vs block size, and draft-step time vs skip
+    fraction (the MLX post's sweep), for the dense workload shapes."""
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    peak, _ = measured_peaks()
+    jobs = [("qwen3-4b", 2048, (1, 2, 3, 4, 6, 8, 12, 16)), ("llama-3.1-8b", 4096, (1, 2, 4, 8, 16)),
+            ("qwen3-8b", 1024, (1, 16)), ("qwen3-8b", 2048, (1, 16)), ("qwen3-8b", 4096, (1, 4, 16))]
+    for name, ctx, ns in jobs:
+        cfg = synth.PRESETS[name](max_ctx=ctx + 64)
+        plan = sv.layer_skip_plan(cfg.n_layers, 0.5)
+        m, _ = _model_at_context(cfg, ctx, plan)
+        for n in ns:
+            us = _verify_us(torch, sv, m, synth.prompt(cfg, n).tolist(), ctx)
+            b = stepmodel.pass_bytes(cfg, n, ctx)
+            _emit({"suite": "verify", "config": name, "ctx": ctx, "n": n, "us": round(us, 1),
+                   "GBps": round(b / us / 1e3, 1), "frac_8TBps": round(b / us / 1e3 / NOMINAL_HBM, 3),
+                   "frac_measured": round(b / us / 1e3 / peak, 3)})
+        if name != "qwen3-8b" or ctx == 2048:
+            for f in (0.1, 0.2, 0.3, 0.4, 0.5):
+                plan = sv.layer_skip_plan(cfg.n_layers, f)
+                m.set_draft_plan(plan)
+                import numpy as np
+                for l in plan:
+                    m.kv_load(1, plan.index(l), synth.synthetic_kv(cfg, l, ctx, 0), synth.synthetic_kv(cfg, l, ctx, 1))
+                m.kv_set_len(1, ctx)
+                us = _draft_us(torch, sv, m, ctx)
+                b = stepmodel.pass_bytes(cfg, 1, ctx, plan)
+                _emit({"suite": "draft", "config": name, "ctx": ctx, "skip_frac": f, "layers": len(plan),
+                       "us": round(us, 1), "GBps": round(b / us / 1e3, 1)})
+        m.close()
+        del m
+        torch.cuda.empty_cache()
+
+
+def suite_geometric(args):
+    """Llama-3.1-8B verify at n = 1..8 with drafts that are seeded corruptions
+    of the target's own greedy tokens (acceptance geometric in alpha); the
+    accepted tokens per second of the verify loop."""
+    import numpy as np
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    ctx = 4096
+    cfg = synth.llama31_8b(max_ctx=ctx + 256)
+    m, _ = _model_at_context(cfg, ctx)
+    # the target's own greedy continuation from the context
+    y = int(synth.prompt(cfg, 1)[0])
+    greedy = [y]
+    blk = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(96):
+        blk.fill_(greedy[-1])
+        am, _, _, _ = m.verify(blk)
+        greedy.append(int(am.item()))
+    for alpha in (0.5, 0.7, 0.9):
+        for n in range(1, 9):
+            m.kv_set_len(0, ctx)
+            pos, toks, cyc = 0, 0, 0
+            am = torch.zeros(n, dtype=torch.int32, device="cuda")
+            ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+            accepts = []
+            t_total = 0.0
+            while pos + n < len(greedy) and cyc < 24:
+                truth = greedy[pos + 1:pos + n]
+                drafts = synth.corrupt_drafts(np.array(truth, dtype=np.int32), alpha, cfg.vocab,
+                                              stream=1000 * n + cyc).tolist() if n > 1 else []
+                b = torch.tensor([greedy[pos]] + drafts, dtype=torch.int32, device="cuda")
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                sv.spec_verify_step(m.h, b, am, ac)
+                sv.spec_kv_rollback(m.h, 0, -1)
+                e1.record()
+                torch.cuda.synchronize()
+                k = int(ac.item())
+                t_total += e0.elapsed_time(e1) * 1e-3
+                accepts.append(k)
+                toks += k + 1
+                pos += k + 1
+                cyc += 1
+            _emit({"suite": "geometric", "config": "llama-3.1-8b", "ctx": ctx, "alpha": alpha, "n": n,
+                   "cycles": cyc, "accept_mean": round(float(np.mean(accepts)), 3),
+                   "expected_tokens": round(stepmodel.tokens_per_verify(alpha, n - 1), 3),
+                   "tokens_per_cycle": round(toks / max(cyc, 1), 3), "us_per_verify": round(t_total / cyc * 1e6, 1),
+                   "accepted_tok_s": round(toks / t_total, 1)})
+    m.close()
+
+
+def suite_dflash(args):
+    """Qwen3-8B verify of a 16-token block (the DFlash block size) at context
+    1024/2048/4096, accept lengths truncated-geometric with mean 6 and 9, then
+    the rollback of the rejected tail."""
+    import numpy as np
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    for ctx in (1024, 2048, 4096):
+        cfg = synth.qwen3_8b(max_ctx=ctx + 64)
+        m, _ = _model_at_context(cfg, ctx)
+        blk = torch.tensor(synth.prompt(cfg, 16).tolist(), dtype=torch.int32, device="cuda")
+        am = torch.zeros(16, dtype=torch.int32, device="cuda")
+        ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+        us_v = _time_calls(torch, lambda: (sv.spec_verify_step(m.h, blk, am, ac), m.kv_set_len(0, ctx)), 10)
+        us_set = _time_calls(torch, lambda: m.kv_set_len(0, ctx), 20)
+        for mean in (6.0, 9.0):
+            alpha = stepmodel.alpha_for_mean_accept(mean, 15)
+            ks = synth.geometric_accept_lengths(64, alpha, 15, stream=int(mean))
+            # the rollback of the rejected tail is timed on its own
+            def rb():
+                for k in ks[:8]:
+                    sv.spec_kv_rollback(m.h, 0, ctx + int(k) + 1)
+                    m.kv_set_len(0, ctx + 16)
+            m.kv_set_len(0, ctx + 16)
+            us_rb = (_time_calls(torch, rb, 5) - 8 * us_set) / 8
+            toks = float(np.mean(ks + 1))
+            t = (us_v - us_set) + max(us_rb, 0.0)
+            b = stepmodel.pass_bytes(cfg, 16, ctx)
+            _emit({"suite": "dflash", "config": "qwen3-8b", "ctx": ctx, "n": 16, "mean_accept": mean,
+                   "alpha": round(alpha, 5), "verify_us": round(us_v - us_set, 1), "rollback_us": round(us_rb, 2),
+                   "GBps": round(b / (us_v - us_set) / 1e3, 1), "tokens_per_cycle": round(toks, 3),
+                   "tok_s": round(toks / t * 1e6, 1)})
+        m.close()
+        torch.cuda.empty_cache()
+
+
+def suite_moe(args):
+    """DeepSeek-V2-Lite-shaped MoE verify at n = 1..8 with forced synthetic
+    routing traces: per-slot vs deduplicated expert reads (time, requested
+    bytes, effective bandwidth), the measured and predicted crossover, and the
+    best draft length over 22 acceptance rates."""
+    import numpy as np
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    ctx = 2048
+    cfg = synth.moe_v2lite(max_ctx=ctx + 64)
+    plan = sv.layer_skip_plan(cfg.n_layers, 0.5)
+    m, _ = _model_at_context(cfg, ctx, plan)
+    L = cfg.n_layers
+    trace = synth.routing_trace(L, 16, cfg.n_experts, cfg.top_k)       # [layer][token][k]
+    m.force_routing(trace)
+    per_expert = stepmodel.expert_bytes(cfg)
+    rows = {}
+    for n in range(1, 9):
+        toks = synth.prompt(cfg, n).tolist()
+        u_layers = [stepmodel.union_size(trace[l, :n]) for l in range(cfg.first_moe_layer, L)]
+        for mode, name in ((sv.SPEC_MOE_PER_SLOT, "per_slot"), (sv.SPEC_MOE_DEDUP, "dedup")):
+            m.moe_mode(mode)
+            us = _verify_us(torch, sv, m, toks, ctx)
+            sv.spec_profile_enable(m.h, True)
+            blk = torch.tensor(toks, dtype=torch.int32, device="cuda")
+            am = torch.zeros(n, dtype=torch.int32, device="cuda")
+            ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+            for _ in range(3):
+                sv.spec_verify_step(m.h, blk, am, ac)
+                sv.spec_kv_rollback(m.h, 0, ctx)
+            g_ms, g_b, g_n = sv.spec_profile_read(m.h, sv.EPI_EXPERT_SWIGLU)
+            d_ms, d_b, d_n = sv.spec_profile_read(m.h, sv.EPI_EXPERT_DOWN)
+            sv.spec_profile_read(m.h, sv.PROF_ALL)
+            sv.spec_profile_enable(m.h, False)
+            exp_us = (g_ms + d_ms) * 1e3 / 3
+            exp_bytes = (g_b + d_b) / 3
+            rows[(n, name)] = (us, exp_us, exp_bytes)
+            _emit({"suite": "moe", "config": "moe-v2-lite", "ctx": ctx, "n": n, "mode": name,
+                   "verify_us": round(us, 1), "expert_us": round(exp_us, 1),
+                   "expert_bytes_requested": int(exp_bytes), "expert_GBps": round(exp_bytes / exp_us / 1e3, 1),
+                   "unique_experts_mean": round(float(np.mean(u_layers)), 2),
+                   "unique_experts_expected": round(stepmodel.union_size_expected(n, cfg.n_experts, cfg.top_k), 2)})
+    # crossover: measured (verify time) and predicted (bytes over bandwidths fitted at one pass size)
+    ns = list(range(1, 9))
+    fit_n = 4
+    b_ps = rows[(fit_n, "per_slot")][2] / rows[(fit_n, "per_slot")][1]
+    b_dd = rows[(fit_n, "dedup")][2] / rows[(fit_n, "dedup")][1]
+    shares = [rows[(n, "dedup")][2] / rows[(n, "per_slot")][2] for n in ns]
+    ratios = [(rows[(n, "dedup")][2] / rows[(n, "dedup")][1]) / (rows[(n, "per_slot")][2] / rows[(n, "per_slot")][1])
+              for n in ns]
+    measured = next((n for n in ns if rows[(n, "dedup")][0] < rows[(n, "per_slot")][0]), None)
+    predicted = stepmodel.first_win(ns, shares, [b_dd / b_ps] * len(ns))
+    _emit({"suite": "moe_crossover", "byte_share_u": [round(x, 3) for x in shares],
+           "bandwidth_ratio_r": [round(x, 3) for x in ratios], "fit_pass_size": fit_n,
+           "r_fit": round(b_dd / b_ps, 3), "crossover_measured": measured, "crossover_predicted": predicted})
+    # best draft length over 22 acceptance rates (verify in the faster mode per n; draft = 50% middle skip)
+    m.moe_mode(sv.SPEC_MOE_DEDUP)
+    t_draft = _draft_us(torch, sv, m, ctx)
+    tv = {n: min(rows[(n, "per_slot")][0], rows[(n, "dedup")][0]) for n in ns}
+    gam = list(range(0, 8))
+    stairs, stairs0 = [], []
+    for a in np.linspace(0.0, 1.0, 22):
+        stairs.append(stepmodel.best_gamma(float(a), lambda k: tv[k], t_draft, gam))
+        stairs0.append(stepmodel.best_gamma(float(a), lambda k: tv[k], 0.0, gam))
+    _emit({"suite": "moe_best_gamma", "draft_us": round(t_draft, 1), "alphas": 22,
+           "best_gamma": stairs, "best_gamma_free_draft": stairs0,
+           "monotone": all(b >= a for a, b in zip(stairs, stairs[1:])),
+           "monotone_free_draft": all(b >= a for a, b in zip(stairs0, stairs0[1:]))})
+    m.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,7 +693,14 @@ def main():
     ap.add_argument("--skip", type=float, default=0.5)
     ap.add_argument("--ctx", type=int, default=2048)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "moe"],
+                    help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
+    if args.suite:
+        import __graft_entry__
+        __graft_entry__.build()
+        {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash, "moe": suite_moe}[args.suite](args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

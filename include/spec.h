@@ -220,16 +220,21 @@ spec_status spec_moe_force_routing(spec_handle h, const int32_t* d_ids);
 /* Number of the library's kernel launches enqueued by the last call. */
 int32_t spec_last_launch_count(spec_handle h);
 
-/* Benchmark hook: while enabled, every dense streaming-GEMM launch is
- * bracketed by CUDA events on the handle's stream (this serialises those
- * launches with their neighbours).  enable = 0 stops recording. */
+/* Benchmark hook: while enabled, every streaming-GEMM launch (and every
+ * persistent pass kernel) is bracketed by CUDA events on the handle's stream
+ * (this serialises those launches with their neighbours).  enable = 0 stops
+ * recording. */
 spec_status spec_profile_enable(spec_handle h, int32_t enable);
 
-/* Synchronise the stream and return, for the GEMM launches recorded since
- * profiling was enabled (or last read): the summed event time in ms, the
- * summed algorithmic bytes (weights + activation operand + outputs, each
- * once) and the launch count.  Resets the record. */
-spec_status spec_profile_read(spec_handle h, double* total_ms, double* total_bytes, int32_t* launches);
+/* Synchronise the stream and return, for the recorded launches of one kind:
+ * the summed event time in ms, the summed bytes and the launch count, and
+ * drop those records.  kind = -1: every dense launch (GEMMs outside the expert
+ * FFN, and pass kernels); -2: all; 0..7: one GEMM epilogue kind; 100: pass
+ * kernels.  Bytes are algorithmic (weights + activation operand + outputs,
+ * each once); for expert launches they are the expert bytes the launch
+ * requests (one expert per (token, slot) in per-slot mode, one per distinct
+ * expert in dedup mode, counted from forced routing ids). */
+spec_status spec_profile_read(spec_handle h, int32_t kind, double* total_ms, double* total_bytes, int32_t* launches);
 
 /* Benchmark hook: while enabled, each persistent pass kernel records, per CTA
  * and phase, four global-timer stamps (phase entered, grid barrier passed,

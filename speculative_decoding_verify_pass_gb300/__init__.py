@@ -88,7 +88,7 @@ def library():
         "spec_moe_force_routing": [vp, vp],
         "spec_last_launch_count": [vp],
         "spec_profile_enable": [vp, i32],
-        "spec_profile_read": [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+        "spec_profile_read": [vp, i32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                               ctypes.POINTER(i32)],
         "spec_accept_from_logits_noalloc": [vp, i32, i32, vp, vp, vp, vp],
         "spec_trace_enable": [vp, i32],
@@ -181,10 +181,14 @@ def spec_profile_enable(h, enable: bool):
     _check(library().spec_profile_enable(h, int(bool(enable))))
 
 
-def spec_profile_read(h):
-    """(total ms, total algorithmic bytes, launches) of the recorded GEMMs."""
+EPI_QKV, EPI_RESID, EPI_SWIGLU, EPI_LMHEAD, EPI_ROUTER, EPI_EXPERT_SWIGLU, EPI_EXPERT_DOWN, EPI_STORE = range(8)
+PROF_DENSE, PROF_ALL, PROF_PASS = -1, -2, 100
+
+
+def spec_profile_read(h, kind: int = PROF_DENSE):
+    """(total ms, total bytes, launches) of the recorded launches of one kind."""
     ms, by, n = ctypes.c_double(0), ctypes.c_double(0), ctypes.c_int32(0)
-    _check(library().spec_profile_read(h, ctypes.byref(ms), ctypes.byref(by), ctypes.byref(n)))
+    _check(library().spec_profile_read(h, int(kind), ctypes.byref(ms), ctypes.byref(by), ctypes.byref(n)))
     return float(ms.value), float(by.value), int(n.value)
 
 

@@ -108,10 +108,19 @@ struct spec_model {
     };
     std::map<int, PassTable> tables;   // (which, n, lm) -> device phase list
     bool profiling = false;
+    bool use_graphs = true;             // replay captured launch sequences (SPEC_GRAPHS=0: direct launches)
+    cudaStream_t cap_stream = nullptr;  // private stream used only for capture
+    struct GraphEntry {
+        cudaGraphExec_t exec;
+        int launches;
+    };
+    std::map<std::vector<uintptr_t>, GraphEntry> graphs;
     struct ProfRec {
         cudaEvent_t a, b;
         double bytes;
+        int kind;   // EPI_* of a GEMM launch, 100 for a whole pass kernel
     };
+    std::vector<int32_t> forced_host;   // host copy of forced routing ids
     std::vector<ProfRec> prof;
     std::vector<void*> allocs;
     std::vector<void*> draft_allocs;
@@ -306,8 +315,24 @@ double gemm_bytes(const GemmParams& p) {
     return w + xin + out;
 }
 
-spec_status gemm(spec_model* h, const GemmParams& p) {
-    const bool rec = h->profiling && !p.items_mode;
+// Expert weight bytes one items-mode launch requests: per-slot reads one
+// expert per (token, slot), dedup one per distinct expert (needs the ids on
+// the host, i.e. forced routing; otherwise the per-slot count is reported).
+double expert_launch_bytes(spec_model* h, const GemmParams& p, int layer) {
+    const double per = (double)p.N * p.KBs * kKBlock * 2.0;
+    const int K = h->c.top_k, n = p.n;
+    int items = n * K;
+    if (p.moe_mode == SPEC_MOE_DEDUP && h->forced_on && !h->forced_host.empty()) {
+        unsigned long long used = 0ull;
+        for (int j = 0; j < n; ++j)
+            for (int s = 0; s < K; ++s) used |= 1ull << (h->forced_host[((size_t)layer * kMaxBlock + j) * K + s] & 63);
+        items = __builtin_popcountll(used);
+    }
+    return items * per + (double)n * p.KBs * kKBlock * 2.0;
+}
+
+spec_status gemm(spec_model* h, const GemmParams& p, int layer = -1) {
+    const bool rec = h->profiling;
     spec_model::ProfRec r{};
     if (rec) {
         CU(cudaEventCreate(&r.a));
@@ -318,7 +343,8 @@ spec_status gemm(spec_model* h, const GemmParams& p) {
     ++h->launches;
     if (rec) {
         CU(cudaEventRecord(r.b, h->stream));
-        r.bytes = gemm_bytes(p);
+        r.bytes = p.items_mode ? expert_launch_bytes(h, p, layer) : gemm_bytes(p);
+        r.kind = p.epi;
         h->prof.push_back(r);
     }
     return SPEC_OK;
@@ -329,12 +355,61 @@ spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, i
                             int32_t* d_accept, float* d_logits, int32_t* d_pair, int32_t* d_token,
                             const int32_t* d_block);
 
+spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode,
+                            int32_t* d_argmax, int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair,
+                            int32_t* d_token, const int32_t* d_block);
+
+void clear_graphs(spec_model* h) {
+    for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second.exec);
+    h->graphs.clear();
+}
+
+// One pass: the persistent pass kernel (opt-in, dense), or the per-phase
+// launch sequence, replayed from a captured CUDA graph when possible.
 spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
                      int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair, int32_t* d_token,
                      const int32_t* d_block) {
-    const spec_model_config& c = h->c;
-    if (h->use_pass && c.n_experts == 0)
+    if (h->use_pass && h->c.n_experts == 0)
         return run_pass_kernel(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_pair, d_token, d_block);
+    if (!h->use_graphs || h->profiling)
+        return run_pass_launch(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_ids, d_pair, d_token,
+                               d_block);
+    const std::vector<uintptr_t> key = {(uintptr_t)which, (uintptr_t)n, (uintptr_t)mode, (uintptr_t)d_tokens,
+                                        (uintptr_t)d_argmax, (uintptr_t)d_accept, (uintptr_t)d_logits,
+                                        (uintptr_t)d_ids, (uintptr_t)d_pair, (uintptr_t)d_token, (uintptr_t)d_block,
+                                        (uintptr_t)h->moe_mode, (uintptr_t)h->forced_on};
+    auto f = h->graphs.find(key);
+    if (f == h->graphs.end()) {
+        if (h->graphs.size() >= 256) clear_graphs(h);
+        cudaStream_t user = h->stream;
+        h->stream = h->cap_stream;
+        h->launches = 0;
+        CU(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+        spec_status s = run_pass_launch(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_ids, d_pair,
+                                        d_token, d_block);
+        cudaGraph_t graph = nullptr;
+        const cudaError_t e = cudaStreamEndCapture(h->cap_stream, &graph);
+        h->stream = user;
+        if (s != SPEC_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return s;
+        }
+        if (e != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaStreamEndCapture: %s", cudaGetErrorString(e));
+        cudaGraphExec_t exec = nullptr;
+        const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (ei != cudaSuccess) return fail(SPEC_ERR_CUDA, "cudaGraphInstantiate: %s", cudaGetErrorString(ei));
+        f = h->graphs.emplace(key, spec_model::GraphEntry{exec, h->launches}).first;
+    }
+    CU(cudaGraphLaunch(f->second.exec, h->stream));
+    h->launches = f->second.launches;
+    return SPEC_OK;
+}
+
+spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode,
+                            int32_t* d_argmax, int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair,
+                            int32_t* d_token, const int32_t* d_block) {
+    const spec_model_config& c = h->c;
     const std::vector<int>& plan = which == 0 ? h->plan_full : h->plan_draft;
     const int d = c.d_model, hd = c.head_dim;
     const int G = h->num_sms;
@@ -443,7 +518,7 @@ spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, P
             p.route_ids = h->route_ids;
             p.xe = h->xe;
             p.xe_stride = h->xe_stride;
-            if ((s = gemm(h, p)) != SPEC_OK) return s;
+            if ((s = gemm(h, p, l)) != SPEC_OK) return s;
             if (c.n_shared_experts > 0) {
                 p = base_params(h, which, n);
                 set_mat(p, W.sdown, h->xs, EPI_STORE, G);
@@ -458,7 +533,7 @@ spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, P
             p.x_item_stride = h->xe_stride;
             p.route_ids = h->route_ids;
             p.y_slot = h->y_slot;
-            if ((s = gemm(h, p)) != SPEC_OK) return s;
+            if ((s = gemm(h, p, l)) != SPEC_OK) return s;
             CombineParams cb{};
             cb.x = h->x;
             cb.y_slot = h->y_slot;
@@ -653,6 +728,7 @@ spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, i
         const size_t layers = which == 0 ? h->plan_full.size() : h->plan_draft.size();
         const double kv = (double)layers * 2.0 * h->c.n_kv_heads * h->c.head_dim * 2.0 * (h->host_len[which] + n);
         r.bytes = tab.gemm_bytes + kv + (double)n * h->c.d_model * 2.0;
+        r.kind = 100;
         CU(cudaEventCreate(&r.a));
         CU(cudaEventCreate(&r.b));
         CU(cudaEventRecord(r.a, h->stream));
@@ -667,6 +743,10 @@ spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, i
 }
 
 void free_all(spec_model* h) {
+    for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second.exec);
+    h->graphs.clear();
+    if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+    h->cap_stream = nullptr;
     if (h->trace) cudaFree(h->trace);
     h->trace = nullptr;
     for (void* p : h->draft_allocs) cudaFree(p);
@@ -741,6 +821,8 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     h->num_sms = prop.multiProcessorCount;
     if (const char* e = std::getenv("SPEC_NO_PDL")) h->pdl = !(e[0] == '1');
     if (const char* e = std::getenv("SPEC_PASS_KERNEL")) h->use_pass = (e[0] == '1');
+    if (const char* e = std::getenv("SPEC_GRAPHS")) h->use_graphs = !(e[0] == '0');
+    TRYCU(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     TRYCU(gemm_configure(h->device));
     TRYCU(pass_configure(h->device));
     TRYCU(attention_configure(h->device));
@@ -895,6 +977,13 @@ spec_status spec_set_draft_plan(spec_handle h, const int32_t* draft_layers, int3
     spec_status s = validate_plan(h, draft_layers, n_draft_layers);
     if (s != SPEC_OK) return s;
     CU(cudaStreamSynchronize(h->stream));
+    clear_graphs(h);
+    for (auto it = h->tables.begin(); it != h->tables.end();) {
+        if (it->first / 10000 == 1)
+            it = h->tables.erase(it);   // draft tables point at the old draft pools
+        else
+            ++it;
+    }
     if ((s = alloc_draft(h, draft_layers, n_draft_layers)) != SPEC_OK) return s;
     h->launches = 0;
     CU(launch_rollback(h->st, 1, 0, h->stream, false));
@@ -1070,6 +1159,7 @@ spec_status spec_moe_force_routing(spec_handle h, const int32_t* d_ids) {
         }
     CU(cudaMemcpyAsync(h->forced, ids.data(), count * sizeof(int32_t), cudaMemcpyHostToDevice, h->stream));
     CU(cudaStreamSynchronize(h->stream));
+    h->forced_host = ids;
     h->forced_on = true;
     return SPEC_OK;
 }
@@ -1108,22 +1198,30 @@ spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int
     return SPEC_OK;
 }
 
-spec_status spec_profile_read(spec_handle h, double* total_ms, double* total_bytes, int32_t* launches) {
+spec_status spec_profile_read(spec_handle h, int32_t kind, double* total_ms, double* total_bytes, int32_t* launches) {
     if (!h || !total_ms || !total_bytes || !launches) return fail(SPEC_ERR_INVALID_ARG, "null argument");
     CU(cudaStreamSynchronize(h->stream));
     double ms = 0.0, bytes = 0.0;
+    int count = 0;
+    std::vector<spec_model::ProfRec> keep;
     for (auto& r : h->prof) {
+        const bool take = kind == -1 ? (r.kind != EPI_EXPERT_SWIGLU && r.kind != EPI_EXPERT_DOWN) : (kind == -2 || r.kind == kind);
+        if (!take) {
+            keep.push_back(r);
+            continue;
+        }
         float t = 0.f;
         CU(cudaEventElapsedTime(&t, r.a, r.b));
         ms += t;
         bytes += r.bytes;
+        ++count;
         cudaEventDestroy(r.a);
         cudaEventDestroy(r.b);
     }
     *total_ms = ms;
     *total_bytes = bytes;
-    *launches = (int32_t)h->prof.size();
-    h->prof.clear();
+    *launches = count;
+    h->prof = keep;
     return SPEC_OK;
 }
 

@@ -126,14 +126,14 @@ __global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ Acc
     if (warp < p.n) {
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        int t = lane;
-        for (; t + 7 * 32 < p.T; t += 8 * 32) {  // eight independent loads in flight per lane
+        for (int t0 = lane; t0 < p.T; t0 += 8 * 32) {  // predicated batches: eight loads in flight per lane
             float v[8];
             int ix[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                v[u] = p.amax_val[warp * p.T + t + u * 32];
-                ix[u] = p.amax_idx[warp * p.T + t + u * 32];
+                const int t = t0 + u * 32;
+                v[u] = t < p.T ? p.amax_val[warp * p.T + t] : -INFINITY;
+                ix[u] = t < p.T ? p.amax_idx[warp * p.T + t] : 0x7fffffff;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -141,14 +141,6 @@ __global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ Acc
                     best = v[u];
                     bi = ix[u];
                 }
-        }
-        for (; t < p.T; t += 32) {
-            const float v = p.amax_val[warp * p.T + t];
-            const int i = p.amax_idx[warp * p.T + t];
-            if (v > best || (v == best && i < bi)) {
-                best = v;
-                bi = i;
-            }
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {

@@ -24,6 +24,7 @@
 // kernel still runs to its end.
 #include <math.h>
 
+#include "attn_core.cuh"
 #include "gemm_core.cuh"
 
 namespace sv {
@@ -191,129 +192,26 @@ __device__ void gemm_phase(const GemmParams& gp, PassSmem& sm, int& q, bool& abo
     }
 }
 
-// One warp: 16 query rows (row group rg) against the 64 keys of one page slab.
-template <int HD>
-__device__ __forceinline__ void attn_warp(const AttnParams& a, const uint16_t* sk, const uint16_t* svv, int h,
-                                          int page_idx, int pos0, int rg, int lane) {
-    const int G = a.n_heads / a.n_kv_heads;
-    const int R = a.n * G;
-    const int g = lane >> 2, cc = lane & 3;
-    const int rA = rg * 16 + g, rB = rA + 8;
-    const uint16_t* qa = rA < R ? a.qbuf + ((size_t)(rA / G) * a.n_heads + h * G + rA % G) * HD : nullptr;
-    const uint16_t* qb = rB < R ? a.qbuf + ((size_t)(rB / G) * a.n_heads + h * G + rB % G) * HD : nullptr;
-    uint32_t qf[HD / 16][4];
-#pragma unroll
-    for (int k16 = 0; k16 < HD / 16; ++k16) {
-        qf[k16][0] = qa ? *reinterpret_cast<const uint32_t*>(qa + k16 * 16 + 2 * cc) : 0u;
-        qf[k16][1] = qb ? *reinterpret_cast<const uint32_t*>(qb + k16 * 16 + 2 * cc) : 0u;
-        qf[k16][2] = qa ? *reinterpret_cast<const uint32_t*>(qa + k16 * 16 + 8 + 2 * cc) : 0u;
-        qf[k16][3] = qb ? *reinterpret_cast<const uint32_t*>(qb + k16 * 16 + 8 + 2 * cc) : 0u;
-    }
-    float s[8][4];
-#pragma unroll
-    for (int n8 = 0; n8 < 8; ++n8) {
-        s[n8][0] = s[n8][1] = s[n8][2] = s[n8][3] = 0.f;
-        const uint16_t* krow = sk + (n8 * 8 + g) * HD;
-#pragma unroll
-        for (int k16 = 0; k16 < HD / 16; ++k16) {
-            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + (((2 * k16) ^ g) << 3) + 2 * cc);
-            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + (((2 * k16 + 1) ^ g) << 3) + 2 * cc);
-            mma_bf16_16816(s[n8], qf[k16], b0, b1);
-        }
-    }
-    const int start = page_idx * kPageSize;
-    const int limA = rA < R ? pos0 + rA / G : -1;
-    const int limB = rB < R ? pos0 + rB / G : -1;
-    float mA = -INFINITY, mB = -INFINITY;
-#pragma unroll
-    for (int n8 = 0; n8 < 8; ++n8)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int kp = start + n8 * 8 + 2 * cc + e;
-            if (kp > limA) s[n8][e] = -INFINITY;
-            if (kp > limB) s[n8][2 + e] = -INFINITY;
-            mA = fmaxf(mA, s[n8][e]);
-            mB = fmaxf(mB, s[n8][2 + e]);
-        }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        mA = fmaxf(mA, __shfl_xor_sync(0xffffffffu, mA, o));
-        mB = fmaxf(mB, __shfl_xor_sync(0xffffffffu, mB, o));
-    }
-    const float k2 = a.scale_log2;
-    const float msA = (mA == -INFINITY) ? -1e30f : mA * k2;
-    const float msB = (mB == -INFINITY) ? -1e30f : mB * k2;
-    float lA = 0.f, lB = 0.f;
-#pragma unroll
-    for (int n8 = 0; n8 < 8; ++n8) {
-        s[n8][0] = exp2f(s[n8][0] * k2 - msA);
-        s[n8][1] = exp2f(s[n8][1] * k2 - msA);
-        s[n8][2] = exp2f(s[n8][2] * k2 - msB);
-        s[n8][3] = exp2f(s[n8][3] * k2 - msB);
-        lA += s[n8][0] + s[n8][1];
-        lB += s[n8][2] + s[n8][3];
-    }
-#pragma unroll
-    for (int o = 1; o <= 2; o <<= 1) {
-        lA += __shfl_xor_sync(0xffffffffu, lA, o);
-        lB += __shfl_xor_sync(0xffffffffu, lB, o);
-    }
-    float o[HD / 8][4];
-#pragma unroll
-    for (int t = 0; t < HD / 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
-    const int mi = lane >> 3, ri = lane & 7;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]), pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
-                                pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
-        const int key = kk * 16 + (mi & 1) * 8 + ri;
-#pragma unroll
-        for (int np = 0; np < HD / 16; ++np) {
-            const int chunk16 = np * 2 + (mi >> 1);
-            uint32_t r[4];
-            ldmatrix_x4_trans(r, smem_u32(svv + key * HD + ((chunk16 ^ ri) << 3)));
-            mma_bf16_16816(o[2 * np], pa, r[0], r[1]);
-            mma_bf16_16816(o[2 * np + 1], pa, r[2], r[3]);
-        }
-    }
-    const size_t base = ((size_t)h * (2 * a.nch) + page_idx) * 64;
-    if (rA < R) {
-        float* dst = a.part_o + (base + rA) * HD;
-#pragma unroll
-        for (int t = 0; t < HD / 8; ++t) *reinterpret_cast<float2*>(dst + t * 8 + 2 * cc) = make_float2(o[t][0], o[t][1]);
-        if (cc == 0) a.part_ml[base + rA] = make_float2(msA, lA);
-    }
-    if (rB < R) {
-        float* dst = a.part_o + (base + rB) * HD;
-#pragma unroll
-        for (int t = 0; t < HD / 8; ++t) *reinterpret_cast<float2*>(dst + t * 8 + 2 * cc) = make_float2(o[t][2], o[t][3]);
-        if (cc == 0) a.part_ml[base + rB] = make_float2(msB, lB);
-    }
-}
-
-// Units (kv head, 128-position chunk); warps 0-3 take page 0 and warps 4-7
-// page 1 of the chunk, each for 16 of the up to 64 query rows.
+// Units (kv head, 128-position chunk) over the ring's four slabs (K and V of
+// the chunk's two pages); see attn_core::attn_unit.
 __device__ void attn_phase(const AttnParams& a, PassSmem& sm, int& q, bool& aborted, int tid, int nc, int pos0,
                            int* err) {
-    const int warp = tid >> 5, lane = tid & 31;
+    const int lane = tid & 31;
     const int U = a.n_kv_heads * nc;
-    const int R = a.n * (a.n_heads / a.n_kv_heads);
     for (int u = blockIdx.x; u < U; u += gridDim.x) {
         const int h = u / nc, c = u % nc;
         for (int t = 0; t < 4; ++t) {
             const int s = (q + t) % kStages;
             if (!aborted && !mbar_wait(&sm.g.full[s], ((q + t) / kStages) & 1, err, 3)) aborted = true;
         }
-        const int half = warp >> 2, rg = warp & 3;
-        if (rg * 16 < R) {
-            const uint16_t* sk = reinterpret_cast<const uint16_t*>(sm.g.w[(q + half) % kStages]);
-            const uint16_t* svv = reinterpret_cast<const uint16_t*>(sm.g.w[(q + 2 + half) % kStages]);
-            if (a.head_dim == 128)
-                attn_warp<128>(a, sk, svv, h, 2 * c + half, pos0, rg, lane);
-            else
-                attn_warp<64>(a, sk, svv, h, 2 * c + half, pos0, rg, lane);
-        }
+        uint16_t* k0 = reinterpret_cast<uint16_t*>(sm.g.w[q % kStages]);
+        uint16_t* k1 = reinterpret_cast<uint16_t*>(sm.g.w[(q + 1) % kStages]);
+        uint16_t* v0 = reinterpret_cast<uint16_t*>(sm.g.w[(q + 2) % kStages]);
+        uint16_t* v1 = reinterpret_cast<uint16_t*>(sm.g.w[(q + 3) % kStages]);
+        if (a.head_dim == 128)
+            attn_core::attn_unit<128>(a, k0, k1, v0, v1, h, c, pos0, tid);
+        else
+            attn_core::attn_unit<64>(a, k0, k1, v0, v1, h, c, pos0, tid);
         __syncwarp();
         if (lane == 0)
             for (int t = 0; t < 4; ++t) mbar_arrive(&sm.g.empty[(q + t) % kStages]);
@@ -321,70 +219,8 @@ __device__ void attn_phase(const AttnParams& a, PassSmem& sm, int& q, bool& abor
     }
 }
 
-// One CTA per (query head, token): merge the 64-position page partials in
-// page order and write the bf16 output into the O projection's operand.
-// Threads split the pages (fixed assignment), partial sums combine in a
-// fixed order, so the result is deterministic and independent of n.
 __device__ void comb_phase(const AttnParams& a, PassSmem& sm, int tid, int nc) {
-    const int G = a.n_heads / a.n_kv_heads;
-    const int HD = a.head_dim;
-    const int np = 2 * nc, NP = 2 * a.nch;
-    const int U = a.n_heads * a.n;
-    const int groups = kConsumers / HD;        // page groups: 2 (hd 128) or 4 (hd 64)
-    const int dim = tid % HD, grp = tid / HD;
-    float* red = sm.g.cs;                      // scratch: [kConsumers] + [groups][HD]
-    for (int u = blockIdx.x; u < U; u += gridDim.x) {
-        const int qh = u % a.n_heads, j = u / a.n_heads;
-        const int h = qh / G, r = j * G + qh % G;
-        const float2* ml = a.part_ml + (size_t)h * NP * 64 + r;
-        float M = -1e30f;
-        for (int pi = tid; pi < np; pi += kConsumers) M = fmaxf(M, ml[(size_t)pi * 64].x);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        if ((tid & 31) == 0) red[tid >> 5] = M;
-        named_bar_sync(1, kConsumers);
-        M = red[0];
-        for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, red[w]);
-        float L = 0.f;
-        for (int pi = tid; pi < np; pi += kConsumers) {
-            const float2 v = ml[(size_t)pi * 64];
-            L += exp2f(v.x - M) * v.y;
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-        named_bar_sync(1, kConsumers);
-        if ((tid & 31) == 0) red[tid >> 5] = L;
-        named_bar_sync(1, kConsumers);
-        L = 0.f;
-        for (int w = 0; w < kConsumerWarps; ++w) L += red[w];
-        // this thread: dimension `dim` over pages grp, grp+groups, ...
-        const float* po = a.part_o + ((size_t)h * NP * 64 + r) * HD + dim;
-        const size_t pstride = (size_t)64 * HD;
-        float O = 0.f;
-        int pi = grp;
-        for (; pi + 7 * groups < np; pi += 8 * groups) {
-            float v[8], m8[8];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                v[t] = po[(size_t)(pi + t * groups) * pstride];
-                m8[t] = ml[(size_t)(pi + t * groups) * 64].x;
-            }
-#pragma unroll
-            for (int t = 0; t < 8; ++t) O += exp2f(m8[t] - M) * v[t];
-        }
-        for (; pi < np; pi += groups) O += exp2f(ml[(size_t)pi * 64].x - M) * po[(size_t)pi * pstride];
-        named_bar_sync(1, kConsumers);
-        red[kConsumers + grp * HD + dim] = O;
-        named_bar_sync(1, kConsumers);
-        if (grp == 0) {
-            float tot = 0.f;
-            for (int gg = 0; gg < groups; ++gg) tot += red[kConsumers + gg * HD + dim];
-            const int k = qh * HD + dim;
-            *reinterpret_cast<uint16_t*>(a.xf_out + (size_t)(k >> 6) * kStageXBytes + xfrag_offset(j, k & 63)) =
-                f2bf(tot / L);
-        }
-        named_bar_sync(1, kConsumers);
-    }
+    attn_core::comb_units(a, sm.g.cs, tid, nc, blockIdx.x, gridDim.x);
 }
 
 __device__ void accept_phase(const PassParams& P, PassSmem& sm, int tid, int pos0) {
@@ -392,14 +228,14 @@ __device__ void accept_phase(const PassParams& P, PassSmem& sm, int tid, int pos
     for (int j = warp; j < P.n; j += kConsumerWarps) {
         float best = -INFINITY;
         int bi = 0x7fffffff;
-        int t = lane;
-        for (; t + 7 * 32 < P.lm_T; t += 8 * 32) {
+        for (int t0 = lane; t0 < P.lm_T; t0 += 8 * 32) {  // predicated batches: eight loads in flight per lane
             float v[8];
             int ix[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-                v[u] = P.amax_val[j * P.lm_T + t + u * 32];
-                ix[u] = P.amax_idx[j * P.lm_T + t + u * 32];
+                const int t = t0 + u * 32;
+                v[u] = t < P.lm_T ? P.amax_val[j * P.lm_T + t] : -INFINITY;
+                ix[u] = t < P.lm_T ? P.amax_idx[j * P.lm_T + t] : 0x7fffffff;
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -407,14 +243,6 @@ __device__ void accept_phase(const PassParams& P, PassSmem& sm, int tid, int pos
                     best = v[u];
                     bi = ix[u];
                 }
-        }
-        for (; t < P.lm_T; t += 32) {
-            const float v = P.amax_val[j * P.lm_T + t];
-            const int i = P.amax_idx[j * P.lm_T + t];
-            if (v > best || (v == best && i < bi)) {
-                best = v;
-                bi = i;
-            }
         }
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {

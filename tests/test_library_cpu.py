@@ -85,3 +85,25 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower().replace("oracles", ""), f
+
+
+def test_step_model_matches_oracle_closed_forms():
+    """The benchmark's product-side step model against the oracle's closed forms."""
+    import numpy as np
+    from speculative_decoding_verify_pass_gb300 import stepmodel as sm
+    for c in (synth.qwen3_4b(), synth.llama31_8b(), synth.qwen3_8b(), synth.tiny()):
+        for n, ctx in ((1, 0), (4, 2048), (16, 4096)):
+            assert sm.pass_bytes(c, n, ctx) == cf.pass_bytes(c, n, ctx).total
+    for a in np.linspace(0, 1, 22):
+        for g in range(0, 16):
+            assert abs(sm.tokens_per_verify(a, g) - cf.expected_tokens(a, g)) < 1e-12
+    for n in range(1, 17):
+        assert abs(sm.union_size_expected(n, 64, 6) - cf.expected_union(n, 64, 6)) < 1e-9
+    tv = lambda n: 1.0 + 0.05 * (n - 1)
+    for a in np.linspace(0, 1, 22):
+        assert sm.best_gamma(a, tv, 0.1, range(16)) == cf.best_draft_length(a, tv, 0.1, range(16))
+    assert abs(sm.mean_accept_truncated(sm.alpha_for_mean_accept(6.0, 15), 15) - 6.0) < 1e-9
+    assert abs(sm.alpha_for_mean_accept(6.0, 15) - 0.87358) < 1e-4
+    assert abs(sm.alpha_for_mean_accept(9.0, 15) - 0.93293) < 1e-4
+    moe = synth.moe_v2lite()
+    assert sm.expert_bytes(moe) == 3 * 1408 * 2048 * 2
