@@ -45,6 +45,46 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+GEMM_SOURCES = ("common.cuh", "internal.h", "gemm_core.cuh", "gemm.cu")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_kernel_dram_qwen3-4b.txt")
+
+
+def gemm_source_sha256():
+    """Digest of the sources the streaming GEMM is compiled from."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "speculative_decoding_verify_pass_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def ncu_traffic(launches_by_kind, cfg, args):
+    """DRAM bytes (read + write) per GEMM launch from the committed ncu
+    capture, averaged over this run's launch mix by epilogue kind; None when
+    the capture is of another workload or of other GEMM sources."""
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None, "no ncu capture committed"
+    per_kind, digest, model = {}, None, None
+    for line in open(TRAFFIC_PROFILE):
+        f = line.split()
+        if len(f) >= 2 and f[0] == "source_sha256":
+            digest = f[1]
+        elif len(f) >= 2 and f[0] == "model":
+            model = f[1]
+        elif len(f) == 6 and f[0] == "kind":
+            per_kind[int(f[1])] = float(f[3]) + float(f[5])
+    if model != cfg.name or args.layers:
+        return None, "ncu capture is of another model"
+    if digest != gemm_source_sha256():
+        return None, "GEMM sources changed since the ncu capture"
+    n = sum(launches_by_kind.values())
+    if n == 0 or any(k not in per_kind for k, c in launches_by_kind.items() if c):
+        return None, "ncu capture lacks a launch kind of this run"
+    tot = sum(per_kind[k] * c for k, c in launches_by_kind.items() if c)
+    return round(tot / n), os.path.relpath(TRAFFIC_PROFILE, ROOT)
+
+
 def pass_bytes(cfg, n, ctx, plan=None):
     from speculative_decoding_verify_pass_gb300 import stepmodel
     return stepmodel.pass_bytes(cfg, n, ctx, plan)
@@ -113,6 +153,8 @@ def build_model(args, torch):
     import synth
     import speculative_decoding_verify_pass_gb300 as sv
     cfg = synth.PRESETS[args.config](max_ctx=args.ctx + 1024)
+    if args.layers:
+        cfg = synth.scaled(cfg, n_layers=args.layers)
     t0 = time.time()
     w = synth.make_weights(cfg)
     t_gen = time.time() - t0
@@ -201,7 +243,9 @@ def run_native(args):
         dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
+    torch.cuda.nvtx.range_push("timed")      # lets a launch-list capture select exactly these launches
     launches = device_cycles(m, torch, gamma, args.steps, buf, acc_log, args.warmup)
+    torch.cuda.nvtx.range_pop()
     e1.record(stream)
     torch.cuda.synchronize()
     if dist:
@@ -246,10 +290,14 @@ def run_native(args):
     # ---- dominant kernel: the streaming GEMM, events around each launch ----
     sv.spec_profile_enable(m.h, True)
     device_cycles(m, torch, gamma, 3, buf, acc_log, total - 3)
-    gms, gbytes, glaunch = sv.spec_profile_read(m.h)
+    per_kind = {k: sv.spec_profile_read(m.h, k) for k in (sv.EPI_QKV, sv.EPI_RESID, sv.EPI_SWIGLU, sv.EPI_LMHEAD)}
     sv.spec_profile_enable(m.h, False)
+    gms = sum(v[0] for v in per_kind.values())
+    gbytes = sum(v[1] for v in per_kind.values())
+    glaunch = sum(v[2] for v in per_kind.values())
     peak, peak_kind = measured_peaks()
     achieved = gbytes / (gms / 1e3) / 1e9 if gms > 0 else 0.0
+    traffic, traffic_note = ncu_traffic({k: v[2] for k, v in per_kind.items()}, cfg, args)
 
     # ---- end to end through the host-driven API (pinned copies each step) ----
     e2e = run_e2e(m, torch, sv, gamma, args, prompt, ctx_now)
@@ -261,7 +309,9 @@ def run_native(args):
         "config": {"workload": "%s self-speculative cycle at context %d (seeded synthetic KV): %d draft steps over the "
                                "%d%% middle-skip plan (%d of %d layers) + verify n=%d + accept + rollback" % (
                                    cfg.name, ctx, gamma, round(args.skip * 100), len(plan), cfg.n_layers, n),
-                   "model": cfg.name + "-shaped, random-init N(0,0.02) bf16", "global_batch": world, "seq_len": ctx,
+                   "model": cfg.name + "-shaped, random-init N(0,0.02) bf16" + (
+                       ", first %d layers only" % args.layers if args.layers else ""),
+                   "global_batch": world, "seq_len": ctx,
                    "gamma": gamma, "skip_frac": args.skip, "draft_layers": len(plan),
                    "l2": "no flush: %.1f GB of weights per cycle exceed the 129 MB L2" % (pass_bytes(cfg, n, ctx) / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -272,7 +322,7 @@ def run_native(args):
                    "by_n": sweep},
         "roofline": {"kernel": "gemm_kernel (weight-streaming GEMM, all dense epilogues)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
                      "launches_timed": glaunch, "bytes_per_launch": round(gbytes / max(glaunch, 1)),
                      "avg_launch_us": round(gms * 1e3 / max(glaunch, 1), 2)},
         "e2e": e2e,
@@ -693,6 +743,8 @@ def main():
     ap.add_argument("--skip", type=float, default=0.5)
     ap.add_argument("--ctx", type=int, default=2048)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="keep only the first N layers (a smaller case for counter captures; the line names it)")
     ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "moe"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()

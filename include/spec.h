@@ -236,15 +236,30 @@ spec_status spec_profile_enable(spec_handle h, int32_t enable);
  * expert in dedup mode, counted from forced routing ids). */
 spec_status spec_profile_read(spec_handle h, int32_t kind, double* total_ms, double* total_bytes, int32_t* launches);
 
-/* Benchmark hook: while enabled, each persistent pass kernel records, per CTA
- * and phase, four global-timer stamps (phase entered, grid barrier passed,
- * phase work done, last streamed stage consumed or 0).  Allocates the trace
- * buffer on enable; synchronous. */
+/* Benchmark hook.  While enabled, every pass records global-timer stamps
+ * (nanoseconds) per CTA:
+ *  - the persistent pass kernel, per phase: phase entered, grid barrier
+ *    passed, phase work done, last streamed stage consumed (or 0);
+ *  - otherwise the pass runs its kernels as separate launches (no graph
+ *    replay) and every GEMM and attention launch records, per CTA: entry,
+ *    inputs ready (after waiting for the previous kernel), main work done
+ *    (GEMM: last weight stage consumed; attention: K/V slabs arrived), exit.
+ *    Stamps a kernel has no point for are 0.
+ * Each pass overwrites the previous record.  Allocates the trace buffer on
+ * enable; synchronous. */
 spec_status spec_trace_enable(spec_handle h, int32_t enable);
 
-/* Copy the last traced pass's stamps ([nctas][nphase][4] nanoseconds) to the
- * host array out (capacity entries).  Synchronises the stream. */
+/* Copy the last traced pass's stamps ([nctas][nphase][4]) to the host array
+ * out (capacity entries).  nphase is the number of phases (pass kernel) or of
+ * traced launches; nctas is the pass kernel's grid, or 512 slots per launch
+ * (unused slots hold zeros).  Synchronises the stream. */
 spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int32_t* nphase, int32_t* nctas);
+
+/* Kind of each traced phase or launch of the last traced pass (count
+ * entries): 0..7 the GEMM epilogue kind (0 QKV, 1 residual, 2 SwiGLU, 3 LM
+ * head, 4 router, 5 expert gate-up, 6 expert down, 7 store), 16 attention
+ * partials, 17 attention chunk merge, 18 embedding, 19 accept. */
+spec_status spec_trace_kinds(spec_handle h, int32_t* out, int32_t capacity, int32_t* count);
 
 /* Greedy accept from caller-computed logits, without any device allocation.
  * The pages have no counterpart to this call.  It serves callers that cannot

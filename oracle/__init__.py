@@ -30,8 +30,8 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
-_LIB = os.path.join(_HERE, "_oracle.so")
-_lib = None
+_LIBS = {False: os.path.join(_HERE, "_oracle.so"), True: os.path.join(_HERE, "_oracle64.so")}
+_lib = {}
 
 (T_EMBED, T_LMHEAD, T_FINALNORM, T_ATTN_NORM, T_FFN_NORM, T_WQ, T_WK, T_WV, T_WO,
  T_GATE, T_UP, T_DOWN, T_ROUTER, T_EGATE, T_EUP, T_EDOWN, T_SGATE, T_SUP, T_SDOWN) = range(19)
@@ -45,20 +45,28 @@ class _Cfg(ctypes.Structure):
                                              "first_moe_layer", "max_ctx")]
 
 
-def build(force: bool = False) -> str:
-    """Compile oracle.c (gcc, OpenMP, no FMA contraction so x86 and Arm agree)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        tmp = _LIB + ".tmp%d" % os.getpid()
-        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
-                               "-o", tmp, _SRC, "-lm"])
-        os.replace(tmp, _LIB)
-    return _LIB
+def build(force: bool = False, acc64: bool = False) -> str:
+    """Compile oracle.c (gcc, OpenMP, no FMA contraction so x86 and Arm agree).
+    ``acc64`` selects the build whose long sums accumulate in fp64."""
+    path = _LIBS[bool(acc64)]
+    if force or not os.path.exists(path) or os.path.getmtime(path) < os.path.getmtime(_SRC):
+        tmp = path + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared"]
+                              + (["-DORC_ACC64"] if acc64 else []) + ["-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, path)
+    return path
 
 
-def _load():
-    global _lib
-    if _lib is None:
-        lib = ctypes.CDLL(build())
+def build_all(force: bool = False) -> None:
+    """Both builds: fp32 accumulation (the oracle) and fp64 accumulation."""
+    build(force, False)
+    build(force, True)
+
+
+def _load(acc64: bool = False):
+    acc64 = bool(acc64)
+    if acc64 not in _lib:
+        lib = ctypes.CDLL(build(acc64=acc64))
         vp, i32 = ctypes.c_void_p, ctypes.c_int
         lib.orc_create.restype = vp
         lib.orc_create.argtypes = [ctypes.POINTER(_Cfg)]
@@ -78,7 +86,7 @@ def _load():
         lib.orc_cache_set_len.restype = i32
         lib.orc_cache_read.argtypes = [vp, i32, i32, i32, vp]
         lib.orc_cache_read.restype = i32
-        lib.orc_forward.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, i32, vp, vp, vp]
+        lib.orc_forward.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp]
         lib.orc_forward.restype = i32
         lib.orc_argmax.argtypes = [vp, i32]
         lib.orc_argmax.restype = i32
@@ -91,8 +99,8 @@ def _load():
         lib.orc_rope.argtypes = [vp, vp, i32]
         lib.orc_attend.argtypes = [vp, vp, vp, i32, i32, i32, i32, vp]
         lib.orc_route.argtypes = [vp, i32, i32, vp, vp, vp]
-        _lib = lib
-    return _lib
+        _lib[acc64] = lib
+    return _lib[acc64]
 
 
 def set_threads(n: int) -> None:
@@ -114,33 +122,34 @@ def _ptr(a: np.ndarray):
 # ----------------------------------------------------------------------------
 # Primitives (the functions the forward is built from), exposed for the pins
 # ----------------------------------------------------------------------------
-def gemm(w_bits: np.ndarray, x: np.ndarray) -> np.ndarray:
-    """Y[i][r] = sum_k W[r][k] X[i][k] in fp32, k in order."""
+def gemm(w_bits: np.ndarray, x: np.ndarray, acc64: bool = False) -> np.ndarray:
+    """Y[i][r] = sum_k W[r][k] X[i][k], k in order, in the build's accumulator."""
     W = np.ascontiguousarray(w_bits, dtype=np.uint16)
     X = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
     N, K = W.shape
     Y = np.empty((X.shape[0], N), dtype=np.float32)
-    _load().orc_gemm(_ptr(W), N, K, _ptr(X), X.shape[0], _ptr(Y))
+    _load(acc64).orc_gemm(_ptr(W), N, K, _ptr(X), X.shape[0], _ptr(Y))
     return Y
 
 
-def rmsnorm(x: np.ndarray, g_bits: np.ndarray, eps: float) -> np.ndarray:
+def rmsnorm(x: np.ndarray, g_bits: np.ndarray, eps: float, acc64: bool = False) -> np.ndarray:
     """bf16(x * rsqrt(mean(x^2) + eps) * g)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     g = np.ascontiguousarray(g_bits, dtype=np.uint16)
     h = np.empty_like(x)
-    _load().orc_rmsnorm(_ptr(x), _ptr(g), x.size, eps, _ptr(h))
+    _load(acc64).orc_rmsnorm(_ptr(x), _ptr(g), x.size, eps, _ptr(h))
     return h
 
 
-def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_heads: int, n_kv_heads: int, head_dim: int):
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_heads: int, n_kv_heads: int, head_dim: int,
+           acc64: bool = False):
     """One token's grouped-query attention over nk cached keys.
     q [Hq*hd]; K, V [nk][Hkv*hd]; returns bf16-rounded [Hq*hd]."""
     q = np.ascontiguousarray(q, dtype=np.float32)
     K = np.ascontiguousarray(K, dtype=np.float32)
     V = np.ascontiguousarray(V, dtype=np.float32)
     out = np.empty(n_heads * head_dim, dtype=np.float32)
-    _load().orc_attend(_ptr(q), _ptr(K), _ptr(V), K.shape[0], n_heads, n_kv_heads, head_dim, _ptr(out))
+    _load(acc64).orc_attend(_ptr(q), _ptr(K), _ptr(V), K.shape[0], n_heads, n_kv_heads, head_dim, _ptr(out))
     return out
 
 
@@ -158,7 +167,7 @@ class Cache:
     """Per-plan KV cache of the oracle (slot s holds layer plan[s])."""
 
     def __init__(self, model: "Oracle", n_slots: int):
-        self._lib = _load()
+        self._lib = model._lib
         self.n_slots = n_slots
         self.model = model
         self.h = self._lib.orc_cache_create(model.h, n_slots)
@@ -198,8 +207,9 @@ class Cache:
 class Oracle:
     """The oracle model over host bf16 weights from ``synth.make_weights``."""
 
-    def __init__(self, cfg, weights):
-        self._lib = _load()
+    def __init__(self, cfg, weights, acc64: bool = False):
+        self._lib = _load(acc64)
+        self.acc64 = bool(acc64)
         self.cfg = cfg
         self.weights = weights      # keeps the host buffers alive
         c = _Cfg(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
@@ -247,9 +257,11 @@ class Oracle:
         return Cache(self, self.cfg.n_layers if n_slots is None else n_slots)
 
     def forward(self, cache: Cache, plan, tokens, pos0: int, logits_from: int | None = 0,
-                want_routing: bool = False, forced_ids=None):
+                want_routing: bool = False, forced_ids=None, probs=None):
         """Run ``tokens`` at positions pos0.. through ``plan``; returns
-        (logits[rows][V] or None, ids or None, gates or None)."""
+        (logits[rows][V] or None, ids or None, gates or None).  ``probs``, a
+        float32 array [len(plan)][n][n_experts], receives the router
+        probabilities of the MoE layers."""
         plan_a = np.ascontiguousarray(plan, dtype=np.int32)
         tok = np.ascontiguousarray(tokens, dtype=np.int32)
         n = len(tok)
@@ -265,12 +277,16 @@ class Oracle:
         if forced_ids is not None:
             forced = np.ascontiguousarray(forced_ids, dtype=np.int32)
             assert forced.shape == (len(plan_a), n, c.top_k)
+        if probs is not None:
+            assert probs.dtype == np.float32 and probs.flags.c_contiguous
+            assert probs.shape == (len(plan_a), n, c.n_experts)
         rc = self._lib.orc_forward(self.h, cache.h, _ptr(plan_a), len(plan_a), _ptr(tok), n, int(pos0),
                                    _ptr(logits) if logits is not None else None,
                                    int(logits_from) if logits is not None else 0,
                                    _ptr(ids) if ids is not None else None,
                                    _ptr(gates) if gates is not None else None,
-                                   _ptr(forced) if forced is not None else None)
+                                   _ptr(forced) if forced is not None else None,
+                                   _ptr(probs) if probs is not None else None)
         if rc != 0:
             raise ValueError("oracle forward rejected its arguments")
         return logits, ids, gates

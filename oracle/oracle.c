@@ -25,6 +25,15 @@
  * Rounding points (bf16 round-to-nearest-even, everything else fp32): the
  * normalised GEMM inputs, q after RoPE, the cached k and v, the attention
  * output and the SwiGLU product.  Logits are fp32.
+ *
+ * Accumulators.  Every long sum (GEMM dot products, the RMSNorm sum of
+ * squares, attention scores, softmax denominators and the weighted value sum)
+ * runs in acc_t: fp32 by default, the precision the pass is specified in.
+ * Built with -DORC_ACC64 the same sums run in fp64 and are rounded to fp32
+ * where the default build holds its fp32 result; every rounding point above is
+ * unchanged.  The two builds compute the same definition; how far they drift
+ * apart measures how reproducible fp32 accumulation is at a given depth and
+ * width, which is what the full-size tests bound an implementation by.
  */
 #include <math.h>
 #include <stdint.h>
@@ -32,6 +41,12 @@
 #include <string.h>
 #ifdef _OPENMP
 #include <omp.h>
+#endif
+
+#ifdef ORC_ACC64
+typedef double acc_t;
+#else
+typedef float acc_t;
 #endif
 
 typedef struct {
@@ -230,18 +245,18 @@ static void gemm_rows(const uint16_t* W, int N, int K, const float* X, int n, fl
         const uint16_t* w = W + (size_t)r * K;
         for (int i = 0; i < n; ++i) {
             const float* x = X + (size_t)i * K;
-            float acc = 0.0f;
-            for (int k = 0; k < K; ++k) acc += bf_widen(w[k]) * x[k];
-            Y[(size_t)i * N + r] = acc;
+            acc_t acc = 0;
+            for (int k = 0; k < K; ++k) acc += (acc_t)bf_widen(w[k]) * x[k];
+            Y[(size_t)i * N + r] = (float)acc;
         }
     }
 }
 
 /* h = bf16(x * rsqrt(mean(x^2) + eps) * g) */
 static void rmsnorm_bf16(const float* x, const uint16_t* g, int d, float eps, float* h) {
-    float ss = 0.0f;
-    for (int k = 0; k < d; ++k) ss += x[k] * x[k];
-    float rstd = 1.0f / sqrtf(ss / (float)d + eps);
+    acc_t ss = 0;
+    for (int k = 0; k < d; ++k) ss += (acc_t)x[k] * x[k];
+    float rstd = 1.0f / sqrtf((float)(ss / (acc_t)d) + eps);
     for (int k = 0; k < d; ++k) h[k] = bf_round(x[k] * rstd * bf_widen(g[k]));
 }
 
@@ -268,20 +283,20 @@ static void attend_one(const float* qv, const float* k0, const float* v0, int st
     float mx = -INFINITY;
     for (int t = 0; t < nk; ++t) {
         const float* kv = k0 + (size_t)t * stride;
-        float dot = 0.0f;
-        for (int e = 0; e < hd; ++e) dot += qv[e] * kv[e];
-        sc[t] = dot * scale;
+        acc_t dot = 0;
+        for (int e = 0; e < hd; ++e) dot += (acc_t)qv[e] * kv[e];
+        sc[t] = (float)dot * scale;
         if (sc[t] > mx) mx = sc[t];
     }
-    float den = 0.0f;
+    acc_t den = 0;
     for (int t = 0; t < nk; ++t) {
         sc[t] = expf(sc[t] - mx);
         den += sc[t];
     }
     for (int e = 0; e < hd; ++e) {
-        float acc = 0.0f;
-        for (int t = 0; t < nk; ++t) acc += sc[t] * v0[(size_t)t * stride + e];
-        out[e] = bf_round(acc / den);
+        acc_t acc = 0;
+        for (int t = 0; t < nk; ++t) acc += (acc_t)sc[t] * v0[(size_t)t * stride + e];
+        out[e] = bf_round((float)(acc / den));
     }
     free(sc);
 }
@@ -291,10 +306,11 @@ static void attend_one(const float* qv, const float* k0, const float* v0, int st
  * (forced ids, when given, replace the pick).  gate = pr[id], not
  * renormalised. */
 static void route_one(float* pr, int E, int K, const int* forced, int* ids, float* gates) {
-    float mx = -INFINITY, den = 0.0f;
+    float mx = -INFINITY;
+    acc_t den = 0;
     for (int e = 0; e < E; ++e) if (pr[e] > mx) mx = pr[e];
     for (int e = 0; e < E; ++e) { pr[e] = expf(pr[e] - mx); den += pr[e]; }
-    for (int e = 0; e < E; ++e) pr[e] = pr[e] / den;
+    for (int e = 0; e < E; ++e) pr[e] = (float)(pr[e] / den);
     char taken[1024];
     memset(taken, 0, sizeof(taken));
     for (int r = 0; r < K; ++r) {
@@ -334,13 +350,15 @@ static void ffn_swiglu(const uint16_t* wg, const uint16_t* wu, const uint16_t* w
  * MoE layers write the chosen expert ids and gates to ids_out / gates_out
  * ([plan_len][n][top_k], may be NULL).  When forced_ids ([plan_len][n][top_k])
  * is given, those ids replace the top-k choice and their gates are the router
- * probabilities at those ids.
+ * probabilities at those ids.  probs_out ([plan_len][n][n_experts], may be
+ * NULL) receives every router probability of every MoE layer, so that a
+ * caller can check a forced choice against the top-k it replaced.
  *
  * Returns 0, or 1 on a bad argument (pos0 beyond the cache length, overflow).
  */
 int orc_forward(const orc_model* m, orc_cache* cache, const int* plan, int plan_len, const int* tokens,
                 int n, int pos0, float* logits, int logits_from, int* ids_out, float* gates_out,
-                const int* forced_ids) {
+                const int* forced_ids, float* probs_out) {
     const orc_cfg* c = &m->c;
     const int d = c->d_model, hd = c->head_dim, Hq = c->n_heads, Hkv = c->n_kv_heads;
     const int qw = Hq * hd, kw = Hkv * hd, group = Hq / Hkv;
@@ -400,6 +418,7 @@ int orc_forward(const orc_model* m, orc_cache* cache, const int* plan, int plan_
                 int chosen[64];
                 float gsel[64];
                 route_one(pr, E, K, forced_ids ? forced_ids + ((size_t)s * n + i) * K : NULL, chosen, gsel);
+                if (probs_out) memcpy(probs_out + ((size_t)s * n + i) * E, pr, sizeof(float) * (size_t)E);
                 for (int r = 0; r < K; ++r) {
                     if (ids_out) ids_out[((size_t)s * n + i) * K + r] = chosen[r];
                     if (gates_out) gates_out[((size_t)s * n + i) * K + r] = gsel[r];

@@ -26,7 +26,7 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_draft_step", "spec_verify_step", "spec_kv_rollback", "spec_moe_mode", "spec_last_error",
             "spec_check_error", "spec_kv_len", "spec_kv_load", "spec_kv_export", "spec_kv_set_len",
             "spec_moe_force_routing", "spec_last_launch_count", "spec_profile_enable", "spec_profile_read",
-            "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read"]
+            "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds"]
 
 
 class SpecError(RuntimeError):
@@ -93,6 +93,7 @@ def library():
         "spec_accept_from_logits_noalloc": [vp, i32, i32, vp, vp, vp, vp],
         "spec_trace_enable": [vp, i32],
         "spec_trace_read": [vp, vp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)],
+        "spec_trace_kinds": [vp, vp, i32, ctypes.POINTER(i32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -196,13 +197,21 @@ def spec_trace_enable(h, enable: bool):
     _check(library().spec_trace_enable(h, int(bool(enable))))
 
 
-def spec_trace_read(h, capacity: int = 152 * 4096 * 4):
+def spec_trace_read(h, capacity: int = 512 * 1216 * 4):
     """Stamps of the last traced pass as an int64 array [ctas][phases][4]."""
     out = np.zeros(capacity, dtype=np.int64)
     nph, nct = ctypes.c_int32(0), ctypes.c_int32(0)
     _check(library().spec_trace_read(h, ctypes.c_void_p(out.ctypes.data), capacity, ctypes.byref(nph),
                                      ctypes.byref(nct)))
     return out[:nct.value * nph.value * 4].reshape(nct.value, nph.value, 4)
+
+
+def spec_trace_kinds(h, capacity: int = 4096):
+    """Kind code of each phase or launch of the last traced pass."""
+    out = np.zeros(capacity, dtype=np.int32)
+    n = ctypes.c_int32(0)
+    _check(library().spec_trace_kinds(h, ctypes.c_void_p(out.ctypes.data), capacity, ctypes.byref(n)))
+    return out[:n.value].copy()
 
 
 def spec_accept_from_logits_noalloc(d_logits, d_block, d_argmax, d_accept_len, stream=None):

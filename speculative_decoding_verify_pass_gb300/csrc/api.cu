@@ -101,10 +101,13 @@ struct spec_model {
     long long* trace = nullptr;         // phase timestamps of the last traced pass
     size_t trace_cap = 0;
     int trace_nphase = 0;
+    int trace_mode = 0;                 // 1: pass-kernel phases, 2: separate launches
+    std::vector<int32_t> trace_kinds;   // per traced phase or launch
     struct PassTable {
         PhaseDesc* dev;
         int count;
         double gemm_bytes;   // algorithmic bytes of the table's GEMM phases
+        std::vector<int32_t> kinds;  // per phase: GEMM epilogue kind, or a kTrace* code
     };
     std::map<int, PassTable> tables;   // (which, n, lm) -> device phase list
     bool profiling = false;
@@ -284,12 +287,13 @@ GemmParams base_params(spec_model* h, int which, int n) {
     return p;
 }
 
-void set_mat(GemmParams& p, const PackedMat& m, const uint8_t* X, int epi, int grid_cap) {
+void set_mat(spec_model* h, GemmParams& p, const PackedMat& m, const uint8_t* X, int epi, int grid_cap) {
     p.W = m.p;
     p.T = m.T;
     p.KBs = m.KBs;
     p.N = m.N;
     p.X = X;
+    p.x_f32 = (X == h->xf_norm) ? 1 : 0;   // normalised operands are kept in fp32
     p.epi = epi;
     p.items_mode = 0;
     const long long I = (long long)m.T * m.KBs;
@@ -302,7 +306,7 @@ void set_mat(GemmParams& p, const PackedMat& m, const uint8_t* X, int epi, int g
 // operand once, the outputs once (fp32 residual read+write for EPI_RESID).
 double gemm_bytes(const GemmParams& p) {
     const double w = (double)p.N * p.KBs * kKBlock * 2.0;
-    const double xin = (double)p.n * p.KBs * kKBlock * 2.0;
+    const double xin = (double)p.n * p.KBs * kKBlock * (p.x_f32 ? 4.0 : 2.0);
     double out = 0.0;
     switch (p.epi) {
         case EPI_QKV: out = (double)p.n * p.N * 2.0; break;
@@ -331,7 +335,19 @@ double expert_launch_bytes(spec_model* h, const GemmParams& p, int layer) {
     return items * per + (double)n * p.KBs * kKBlock * 2.0;
 }
 
-spec_status gemm(spec_model* h, const GemmParams& p, int layer = -1) {
+// Next launch slot of a traced pass (nullptr when not tracing or full).
+long long* trace_slot(spec_model* h, int kind, int slots = 1) {
+    if (!h->trace || h->trace_mode != 2) return nullptr;
+    const size_t per = (size_t)kTraceCtas * 4;
+    if ((h->trace_kinds.size() + slots) * per > h->trace_cap) return nullptr;
+    long long* t = h->trace + h->trace_kinds.size() * per;
+    for (int i = 0; i < slots; ++i) h->trace_kinds.push_back(kind + i);
+    return t;
+}
+
+spec_status gemm(spec_model* h, const GemmParams& p_in, int layer = -1) {
+    GemmParams p = p_in;
+    p.trace = trace_slot(h, p.epi);
     const bool rec = h->profiling;
     spec_model::ProfRec r{};
     if (rec) {
@@ -371,6 +387,13 @@ spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, P
                      const int32_t* d_block) {
     if (h->use_pass && h->c.n_experts == 0)
         return run_pass_kernel(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_pair, d_token, d_block);
+    if (h->trace) {  // a traced pass runs its launches directly, each with its own stamp slots
+        h->trace_mode = 2;
+        h->trace_kinds.clear();
+        CU(cudaMemsetAsync(h->trace, 0, h->trace_cap * sizeof(long long), h->stream));
+        return run_pass_launch(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_ids, d_pair, d_token,
+                               d_block);
+    }
     if (!h->use_graphs || h->profiling)
         return run_pass_launch(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_ids, d_pair, d_token,
                                d_block);
@@ -442,7 +465,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
 
         // QKV (attn RMSNorm scale, RoPE, paged KV append)
         GemmParams p = base_params(h, which, n);
-        set_mat(p, W.qkv, h->xf_norm, EPI_QKV, G);
+        set_mat(h, p, W.qkv, h->xf_norm, EPI_QKV, G);
         p.norm_dim = d;
         p.rope = h->rope;
         p.qbuf = h->qbuf;
@@ -467,24 +490,25 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         a.head_dim = hd;
         a.nch = h->nch;
         a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+        a.trace = trace_slot(h, kTraceAttnPartial, 2);
         CU(launch_attention(a, h->stream, pdl));
         h->launches += 2;
 
         // O projection + residual; next operand = ffn-normed x
         p = base_params(h, which, n);
-        set_mat(p, W.o, h->xf_o, EPI_RESID, G);
+        set_mat(h, p, W.o, h->xf_o, EPI_RESID, G);
         p.g_next = W.ffn_norm;
         p.xf_out = h->xf_norm;
         if ((s = gemm(h, p)) != SPEC_OK) return s;
 
         if (!W.moe) {
             p = base_params(h, which, n);
-            set_mat(p, W.gu, h->xf_norm, EPI_SWIGLU, G);
+            set_mat(h, p, W.gu, h->xf_norm, EPI_SWIGLU, G);
             p.norm_dim = d;
             p.xf_out = h->xf_down;
             if ((s = gemm(h, p)) != SPEC_OK) return s;
             p = base_params(h, which, n);
-            set_mat(p, W.down, h->xf_down, EPI_RESID, G);
+            set_mat(h, p, W.down, h->xf_down, EPI_RESID, G);
             p.g_next = g_after;
             p.xf_out = h->xf_norm;
             if ((s = gemm(h, p)) != SPEC_OK) return s;
@@ -492,7 +516,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             const int K = c.top_k;
             // router: softmax + top-k
             p = base_params(h, which, n);
-            set_mat(p, W.router, h->xf_norm, EPI_ROUTER, G);
+            set_mat(h, p, W.router, h->xf_norm, EPI_ROUTER, G);
             p.norm_dim = d;
             p.route_ids = h->route_ids;
             p.route_gates = h->route_gates;
@@ -502,14 +526,14 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             // shared experts (dense SwiGLU over all tokens)
             if (c.n_shared_experts > 0) {
                 p = base_params(h, which, n);
-                set_mat(p, W.sgu, h->xf_norm, EPI_SWIGLU, G);
+                set_mat(h, p, W.sgu, h->xf_norm, EPI_SWIGLU, G);
                 p.norm_dim = d;
                 p.xf_out = h->xs;
                 if ((s = gemm(h, p)) != SPEC_OK) return s;
             }
             // routed experts, gate/up: per-slot or deduplicated work items
             p = base_params(h, which, n);
-            set_mat(p, W.egu, h->xf_norm, EPI_EXPERT_SWIGLU, G);
+            set_mat(h, p, W.egu, h->xf_norm, EPI_EXPERT_SWIGLU, G);
             p.items_mode = 1;
             p.grid = G;
             p.w_item_stride = W.egu_stride;
@@ -521,12 +545,12 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             if ((s = gemm(h, p, l)) != SPEC_OK) return s;
             if (c.n_shared_experts > 0) {
                 p = base_params(h, which, n);
-                set_mat(p, W.sdown, h->xs, EPI_STORE, G);
+                set_mat(h, p, W.sdown, h->xs, EPI_STORE, G);
                 p.y_store = h->ys;
                 if ((s = gemm(h, p)) != SPEC_OK) return s;
             }
             p = base_params(h, which, n);
-            set_mat(p, W.edown, h->xe, EPI_EXPERT_DOWN, G);
+            set_mat(h, p, W.edown, h->xe, EPI_EXPERT_DOWN, G);
             p.items_mode = 1;
             p.grid = G;
             p.w_item_stride = W.edown_stride;
@@ -556,7 +580,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         return SPEC_OK;
     }
     GemmParams p = base_params(h, which, n);
-    set_mat(p, h->lm, h->xf_norm, EPI_LMHEAD, G);
+    set_mat(h, p, h->lm, h->xf_norm, EPI_LMHEAD, G);
     p.norm_dim = d;
     p.logits = d_logits;
     p.amax_val = h->amax_val;
@@ -638,7 +662,7 @@ spec_status pass_table(spec_model* h, int which, int n, bool lm, spec_model::Pas
         uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
         uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
         GemmParams p = base_params(h, which, n);
-        set_mat(p, W.qkv, h->xf_norm, EPI_QKV, G);
+        set_mat(h, p, W.qkv, h->xf_norm, EPI_QKV, G);
         p.norm_dim = d;
         p.rope = h->rope;
         p.qbuf = h->qbuf;
@@ -649,24 +673,24 @@ spec_status pass_table(spec_model* h, int which, int n, bool lm, spec_model::Pas
         phase(PH_ATTN).a = attn_params(h, which, n, kpool, vpool);
         phase(PH_COMB).a = attn_params(h, which, n, kpool, vpool);
         p = base_params(h, which, n);
-        set_mat(p, W.o, h->xf_o, EPI_RESID, G);
+        set_mat(h, p, W.o, h->xf_o, EPI_RESID, G);
         p.g_next = W.ffn_norm;
         p.xf_out = h->xf_norm;
         phase(PH_GEMM).g = p;
         p = base_params(h, which, n);
-        set_mat(p, W.gu, h->xf_norm, EPI_SWIGLU, G);
+        set_mat(h, p, W.gu, h->xf_norm, EPI_SWIGLU, G);
         p.norm_dim = d;
         p.xf_out = h->xf_down;
         phase(PH_GEMM).g = p;
         p = base_params(h, which, n);
-        set_mat(p, W.down, h->xf_down, EPI_RESID, G);
+        set_mat(h, p, W.down, h->xf_down, EPI_RESID, G);
         p.g_next = g_after;
         p.xf_out = h->xf_norm;
         phase(PH_GEMM).g = p;
     }
     if (lm) {
         GemmParams p = base_params(h, which, n);
-        set_mat(p, h->lm, h->xf_norm, EPI_LMHEAD, G);
+        set_mat(h, p, h->lm, h->xf_norm, EPI_LMHEAD, G);
         p.norm_dim = d;
         p.amax_val = h->amax_val;
         p.amax_idx = h->amax_idx;
@@ -683,7 +707,12 @@ spec_status pass_table(spec_model* h, int which, int n, bool lm, spec_model::Pas
     double gb = 0.0;
     for (const PhaseDesc& ph : v)
         if (ph.kind == PH_GEMM) gb += gemm_bytes(ph.g);
-    h->tables[key] = {dev, (int)v.size(), gb};
+    std::vector<int32_t> kinds;
+    for (const PhaseDesc& ph : v)
+        kinds.push_back(ph.kind == PH_GEMM ? ph.g.epi : ph.kind == PH_ATTN ? kTraceAttnPartial
+                        : ph.kind == PH_COMB ? kTraceAttnCombine : ph.kind == PH_EMBED ? kTraceEmbed
+                        : kTraceAccept);
+    h->tables[key] = {dev, (int)v.size(), gb, kinds};
     *out = h->tables[key];
     return SPEC_OK;
 }
@@ -719,6 +748,8 @@ spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, i
         if (need <= h->trace_cap) {
             P.trace = h->trace;
             h->trace_nphase = tab.count;
+            h->trace_mode = 1;
+            h->trace_kinds = tab.kinds;
         }
     }
     spec_model::ProfRec r{};
@@ -932,7 +963,7 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     // ---- activations and scratch ----
     const int ffn_max = std::max(c.ffn_dim, 64);
     TRY(dalloc_t(h, &h->x, (size_t)kMaxBlock * d));
-    TRY(dalloc_t(h, &h->xf_norm, (size_t)(d / kKBlock) * kStageXBytes));
+    TRY(dalloc_t(h, &h->xf_norm, (size_t)(d / kKBlock) * kStageX32Bytes));
     TRY(dalloc_t(h, &h->xf_o, (size_t)(qw / kKBlock) * kStageXBytes));
     TRY(dalloc_t(h, &h->xf_down, (size_t)(ffn_max / kKBlock) * kStageXBytes));
     TRY(dalloc_t(h, &h->qbuf, (size_t)kMaxBlock * qw));
@@ -1188,13 +1219,39 @@ spec_status spec_trace_enable(spec_handle h, int32_t enable) {
 
 spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int32_t* nphase, int32_t* nctas) {
     if (!h || !out || !nphase || !nctas) return fail(SPEC_ERR_INVALID_ARG, "null argument");
-    if (!h->trace || h->trace_nphase == 0) return fail(SPEC_ERR_STATE, "no traced pass");
-    const size_t count = (size_t)h->num_sms * h->trace_nphase * 4;
-    if ((size_t)capacity < count) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", count);
+    if (!h->trace || h->trace_mode == 0) return fail(SPEC_ERR_STATE, "no traced pass");
     CU(cudaStreamSynchronize(h->stream));
-    CU(cudaMemcpy(out, h->trace, count * sizeof(long long), cudaMemcpyDeviceToHost));
-    *nphase = h->trace_nphase;
-    *nctas = h->num_sms;
+    if (h->trace_mode == 1) {
+        if (h->trace_nphase == 0) return fail(SPEC_ERR_STATE, "no traced pass");
+        const size_t count = (size_t)h->num_sms * h->trace_nphase * 4;
+        if ((size_t)capacity < count) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", count);
+        CU(cudaMemcpy(out, h->trace, count * sizeof(long long), cudaMemcpyDeviceToHost));
+        *nphase = h->trace_nphase;
+        *nctas = h->num_sms;
+        return SPEC_OK;
+    }
+    // separate launches: device layout [launch][kTraceCtas][4] -> [kTraceCtas][launch][4]
+    const size_t nl = h->trace_kinds.size();
+    if (nl == 0) return fail(SPEC_ERR_STATE, "no traced pass");
+    const size_t count = (size_t)kTraceCtas * nl * 4;
+    if ((size_t)capacity < count) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", count);
+    std::vector<long long> dev(count);
+    CU(cudaMemcpy(dev.data(), h->trace, count * sizeof(long long), cudaMemcpyDeviceToHost));
+    for (size_t l = 0; l < nl; ++l)
+        for (size_t c = 0; c < (size_t)kTraceCtas; ++c)
+            for (int k = 0; k < 4; ++k) out[(c * nl + l) * 4 + k] = dev[(l * kTraceCtas + c) * 4 + k];
+    *nphase = (int32_t)nl;
+    *nctas = kTraceCtas;
+    return SPEC_OK;
+}
+
+spec_status spec_trace_kinds(spec_handle h, int32_t* out, int32_t capacity, int32_t* count) {
+    if (!h || !out || !count) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (!h->trace || h->trace_mode == 0) return fail(SPEC_ERR_STATE, "no traced pass");
+    const size_t nl = h->trace_kinds.size();
+    if ((size_t)capacity < nl) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", nl);
+    for (size_t i = 0; i < nl; ++i) out[i] = h->trace_kinds[i];
+    *count = (int32_t)nl;
     return SPEC_OK;
 }
 

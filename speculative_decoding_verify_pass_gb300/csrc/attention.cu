@@ -10,7 +10,8 @@
 //    bank-conflict free);
 //  * 8 warps: 4 groups of 16 of the n*G query rows (G query heads per kv
 //    head, <= 64 rows) times the chunk's 2 pages; S = Q K^T and O = P V run
-//    on bf16 tensor-core MMA with fp32 accumulation, P rounded to bf16;
+//    on bf16 tensor-core MMA with fp32 accumulation, P as a bf16 high part
+//    plus a bf16 low part;
 //  * the two pages of a row group merge in shared memory and the CTA writes
 //    one (row max, row sum, unnormalised O) per row; a merge kernel (one CTA
 //    per query head and token) combines the chunks in increasing order.
@@ -36,42 +37,64 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const __grid
 
     const int h = blockIdx.x, chunk = blockIdx.y;
     const int tid = threadIdx.x;
-    pdl_launch_dependents();
-    pdl_wait();
+    const int cta = chunk * gridDim.x + h;
+    long long* tr = (p.trace && cta < kTraceCtas && tid == 0) ? p.trace + (size_t)cta * 4 : nullptr;
+    if (tr) tr[0] = trace_clock();
+    // The cache length and the keys/values of positions before it were
+    // written by kernels that completed before the preceding QKV kernel
+    // passed its own dependency wait, so they may be read before ours; only
+    // the block's new rows (positions >= pos0) come from the QKV kernel.
     const int pos0 = p.st->len[p.which];
     const int total = pos0 + p.n;
     const int start = chunk * kAttnChunk;
-    if (start >= total) return;
-    if (total > p.nch * kAttnChunk) {  // positions beyond the allocated pages
-        if (tid == 0) atomicCAS(&p.st->error, 0, 20);
+    if (start >= total || total > p.nch * kAttnChunk) {
+        pdl_wait();
+        pdl_launch_dependents();
+        if (total > p.nch * kAttnChunk && tid == 0) atomicCAS(&p.st->error, 0, 20);  // beyond the pages
+        if (tr) tr[3] = trace_clock();
         return;
     }
     constexpr uint32_t kSlab = kPageSize * HD * 2;
+    auto issue = [&](int pg) {
+        const int page = p.block_table[start / kPageSize + pg];
+        const size_t off = ((size_t)(page * p.n_kv_heads + h) * kPageSize) * HD;
+        bulk_g2s(sk + pg * kPageSize * HD, p.kpool + off, kSlab, &bar);
+        bulk_g2s(svv + pg * kPageSize * HD, p.vpool + off, kSlab, &bar);
+    };
     if (tid == 0) {
         mbar_init(&bar, 1);
         fence_barrier_init();
         mbar_arrive_expect_tx(&bar, 4 * kSlab);
-        for (int pg = 0; pg < 2; ++pg) {
-            const int page = p.block_table[start / kPageSize + pg];
-            const size_t off = ((size_t)(page * p.n_kv_heads + h) * kPageSize) * HD;
-            bulk_g2s(sk + pg * kPageSize * HD, p.kpool + off, kSlab, &bar);
-            bulk_g2s(svv + pg * kPageSize * HD, p.vpool + off, kSlab, &bar);
-        }
+        for (int pg = 0; pg < 2; ++pg)
+            if (start + (pg + 1) * kPageSize <= pos0) issue(pg);  // fully cached page: load now
     }
+    pdl_wait();
+    pdl_launch_dependents();
+    if (tr) tr[1] = trace_clock();
+    if (tid == 0)
+        for (int pg = 0; pg < 2; ++pg)
+            if (start + (pg + 1) * kPageSize > pos0) issue(pg);   // holds new rows
     __syncthreads();
     mbar_wait(&bar, 0, &p.st->error, 3);
+    if (tr) tr[2] = trace_clock();
     attn_core::attn_unit<HD>(p, sk, sk + kPageSize * HD, svv, svv + kPageSize * HD, h, chunk, pos0, tid);
+    if (tr) tr[3] = trace_clock();
 }
 
 // One CTA per (query head, token): the page partials merged in page order.
 __global__ void __launch_bounds__(attn_core::kAttnCombThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
     __shared__ float red[3 * attn_core::kMaxChunks];
-    pdl_launch_dependents();
+    long long* tr = (p.trace && blockIdx.x < kTraceCtas && threadIdx.x == 0)
+                        ? p.trace + (size_t)(kTraceCtas + blockIdx.x) * 4 : nullptr;
+    if (tr) tr[0] = trace_clock();
     pdl_wait();
+    pdl_launch_dependents();
+    if (tr) tr[1] = trace_clock();
     const int total = p.st->len[p.which] + p.n;
     int nc = (total + kAttnChunk - 1) / kAttnChunk;
     if (nc > p.nch) nc = p.nch;
     attn_core::comb_units(p, red, threadIdx.x, nc, blockIdx.x, gridDim.x);
+    if (tr) tr[3] = trace_clock();
 }
 
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void** args) {

@@ -3,7 +3,8 @@
 //
 // A unit is (kv head h, 128-position chunk c).  Its 8 warps split the work as
 // 4 groups of 16 query rows x the chunk's 2 pages of 64 keys; each warp runs
-// S = Q K^T and O = P V on bf16 tensor-core MMA with fp32 accumulation.  The
+// S = Q K^T and O = P V on bf16 tensor-core MMA with fp32 accumulation (P as
+// a bf16 high part plus a bf16 low part, ~16 significant bits).  The
 // two pages of a row group are then merged in shared memory (page 0 first)
 // and the unit writes one partial (row max, row sum, unnormalised O) per row:
 // partials are indexed by absolute chunk, so a query's result never depends on
@@ -94,19 +95,31 @@ __device__ __forceinline__ void attn_rows(const AttnParams& a, const uint16_t* s
 #pragma unroll
     for (int t = 0; t < HD / 8; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
     const int mi = lane >> 3, ri = lane & 7;
+    // P = P_hi + P_lo, both bf16: two MMAs keep ~16 bits of the fp32 weights
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-        const uint32_t pa[4] = {pack_bf16x2(s[2 * kk][0], s[2 * kk][1]), pack_bf16x2(s[2 * kk][2], s[2 * kk][3]),
-                                pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+        float hi[8], lo[8];
+        const float src[8] = {s[2 * kk][0], s[2 * kk][1], s[2 * kk][2], s[2 * kk][3],
+                              s[2 * kk + 1][0], s[2 * kk + 1][1], s[2 * kk + 1][2], s[2 * kk + 1][3]};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            hi[e] = bf_round(src[e]);
+            lo[e] = src[e] - hi[e];
+        }
+        const uint32_t ph[4] = {pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]), pack_bf16x2(hi[4], hi[5]),
+                                pack_bf16x2(hi[6], hi[7])};
+        const uint32_t pl[4] = {pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                                pack_bf16x2(lo[6], lo[7])};
         const int key = kk * 16 + (mi & 1) * 8 + ri;
 #pragma unroll
         for (int np = 0; np < HD / 16; ++np) {
             const int chunk16 = np * 2 + (mi >> 1);
             uint32_t r[4];
             ldmatrix_x4_trans(r, smem_u32(svv + key * HD + ((chunk16 ^ ri) << 3)));
-            mma_bf16_16816(o[2 * np], pa, r[0], r[1]);
-            mma_bf16_16816(o[2 * np + 1], pa, r[2], r[3]);
+            mma_bf16_16816(o[2 * np], ph, r[0], r[1]);
+            mma_bf16_16816(o[2 * np + 1], ph, r[2], r[3]);
+            mma_bf16_16816(o[2 * np], pl, r[0], r[1]);
+            mma_bf16_16816(o[2 * np + 1], pl, r[2], r[3]);
         }
     }
 }

@@ -16,7 +16,8 @@ constexpr int kMaxBlock = 16;        // tokens per pass (verify block n <= 16)
 constexpr int kTileRows = 128;       // weight rows per streamed tile
 constexpr int kKBlock = 64;          // k elements per streamed stage
 constexpr int kStageWBytes = kTileRows * kKBlock * 2;   // 16 KB of weights
-constexpr int kStageXBytes = kMaxBlock * kKBlock * 2;   // 2 KB of activations
+constexpr int kStageXBytes = kMaxBlock * kKBlock * 2;   // 2 KB of bf16 activations
+constexpr int kStageX32Bytes = kMaxBlock * kKBlock * 4; // 4 KB of fp32 activations (normalised operands)
 constexpr int kPageSize = 64;        // KV positions per page
 constexpr int kAttnChunk = 128;      // positions per attention work item
 constexpr int kMaxExperts = 64;
@@ -50,6 +51,25 @@ __device__ __forceinline__ int xfrag_offset(int j, int kk) {
     const int half = kin >> 3, c = (kin & 7) >> 1, e = kin & 1;
     const int lane = g * 4 + c;
     return (((n8 * 4 + k16) * 32 + lane) * 8) + half * 4 + e * 2;
+}
+
+// fp32 variant for operands that a normalisation scales before rounding:
+// [n8 tile][k16][lane][b0, b1, b2, b3 as floats], 16 bytes per lane.
+__device__ __forceinline__ int xfrag32_offset(int j, int kk) {
+    const int n8 = j >> 3, g = j & 7;
+    const int k16 = kk >> 4, kin = kk & 15;
+    const int half = kin >> 3, c = (kin & 7) >> 1, e = kin & 1;
+    const int lane = g * 4 + c;
+    return (((n8 * 4 + k16) * 32 + lane) * 16) + (half * 2 + e) * 4;
+}
+
+// Bytes of one operand stage (n rows, bf16 or fp32) and one k-block's stride.
+__host__ __device__ __forceinline__ uint32_t x_stage_bytes(int n, int f32) {
+    const uint32_t base = n > 8 ? (uint32_t)kStageXBytes : (uint32_t)(kStageXBytes / 2);
+    return f32 ? 2 * base : base;
+}
+__host__ __device__ __forceinline__ long long x_kblock_stride(int f32) {
+    return f32 ? (long long)kStageX32Bytes : (long long)kStageXBytes;
 }
 
 // Element offset of (key slot, dim) inside one KV page slab [64][hd]: 16-byte

@@ -12,15 +12,18 @@
 //    mma.m16n8k16 A-fragment order, so a stage is one contiguous 1-D bulk copy
 //    (TMA engine, mbarrier completion) and each consumer lane reads its
 //    fragment with one 16-byte shared load.
-//  * The activation operand (n x 64 per stage, <= 2 KB) is kept by the
-//    producing kernel in B-fragment order and bulk-copied next to the weights.
-//  * An 11-deep ring of stages keeps 176 KB of weights in flight per SM.  The
+//  * The activation operand (n x 64 per stage) is kept by the producing kernel
+//    in B-fragment order and bulk-copied next to the weights: bf16 (<= 2 KB)
+//    for plain operands, fp32 x*gain (<= 4 KB) for RMS-normalised ones, which
+//    the consumers scale by rstd and round to bf16 while building fragments.
+//  * A 10-deep ring of stages keeps 160 KB of weights in flight per SM.  The
 //    CTA takes over half of the SM's shared memory on purpose: a persistent
 //    grid with a static split must not have two of its CTAs on one SM.
 //  * Work split: stream-K over the flattened (tile, k-block) space, each CTA
-//    one contiguous range; a tile split between CTAs is summed by the last CTA
-//    to arrive, in fixed contributor order (deterministic, and independent of
-//    n, so row i of a verify pass equals a one-token decode bitwise).  MoE
+//    one contiguous range; a tile split between CTAs is summed by its first
+//    contributor (for which it is the last segment), in fixed contributor
+//    order (deterministic, and independent of n, so row i of a verify pass
+//    equals a one-token decode bitwise).  MoE
 //    expert GEMMs instead take whole (item, tile) units, so per-slot and
 //    deduplicated schedules share every reduction order.
 //  * The fused epilogue (RMSNorm scale, RoPE + paged KV append, residual add,
@@ -45,6 +48,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int* err = &p.st->error;
+    long long* tr = (p.trace && blockIdx.x < kTraceCtas) ? p.trace + (size_t)blockIdx.x * 4 : nullptr;
+    if (tr && tid == 0) tr[0] = trace_clock();
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -54,15 +59,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         fence_barrier_init();
     }
     __syncthreads();
-    pdl_launch_dependents();
 
     if (p.items_mode) {  // the work list depends on the router's output
         pdl_wait();
+        pdl_launch_dependents();
         if (tid == 0) build_items(p, sm);
         __syncthreads();
     }
     const int n_items = p.items_mode ? sm.n_items : 0;
-    const uint32_t xb = p.n > 8 ? (uint32_t)kStageXBytes : (uint32_t)(kStageXBytes / 2);
+    const uint32_t xb = x_stage_bytes(p.n, p.x_f32);
+    const long long xstride = x_kblock_stride(p.x_f32);
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one lane issues every bulk copy ----------------
@@ -76,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 return p.W + e * p.w_item_stride + ((long long)s.tile * p.KBs + s.b) * kStageWBytes;
             };
             auto x_src = [&](const StageIter& s) {
-                return p.X + (long long)s.item * p.x_item_stride + (long long)s.b * kStageXBytes;
+                return p.X + (long long)s.item * p.x_item_stride + (long long)s.b * xstride;
             };
             if (!p.items_mode) {
                 // weights do not depend on the previous kernel: start streaming them now
@@ -90,8 +96,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     it.advance();
                 }
                 pdl_wait();
+                pdl_launch_dependents();
                 for (int i = 0; i < pre; ++i)
-                    bulk_g2s(sm.x[i], p.X + (long long)pre_b[i] * kStageXBytes, xb, &sm.full[i]);
+                    bulk_g2s(sm.x[i], p.X + (long long)pre_b[i] * xstride, xb, &sm.full[i]);
                 q = pre;
             }
             while (it.valid) {
@@ -110,12 +117,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 
     // -------------------- consumers: 8 warps, 16 weight rows each --------------------
-    if (!p.items_mode) pdl_wait();
+    if (!p.items_mode) {
+        pdl_wait();
+        pdl_launch_dependents();
+    }
     compute_rstd(p, sm, tid);
+    if (tr && tid == 0) tr[1] = trace_clock();
 
     StageIter it;
     it.init(p, n_items);
     const bool two = p.n > 8;
+    const bool f32 = p.x_f32 != 0;
+    const float ra0 = sm.rstd_op[lane >> 2], ra1 = sm.rstd_op[8 + (lane >> 2)];
     int q = 0;
     bool aborted = false;
 
@@ -125,29 +138,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         for (int b = b0; b < b1; ++b, ++q) {
             const int s = q % kStages;
             if (!aborted && !mbar_wait(&sm.full[s], (q / kStages) & 1, err, 1)) aborted = true;
-            const uint8_t* ws = sm.w[s] + warp * 2048 + lane * 16;
-            const uint8_t* xs = sm.x[s] + lane * 8;
-#pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-                const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
-                const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-                const uint2 bv = *reinterpret_cast<const uint2*>(xs + k16 * 256);
-                mma_bf16_16816(acc0, a, bv.x, bv.y);
-                if (two) {
-                    const uint2 bw = *reinterpret_cast<const uint2*>(xs + 1024 + k16 * 256);
-                    mma_bf16_16816(acc1, a, bw.x, bw.y);
-                }
-            }
+            mma_stage(sm, s, warp, lane, two, f32, ra0, ra1, acc0, acc1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
         }
         // the segment of the CTA's range that lies in this tile is done
         it.valid = it.next_seg();
+        if (tr && tid == 0 && !it.valid) tr[2] = trace_clock();
 
         if (!finish_tile(p, sm, tile, b0, b1, acc0, acc1, tid)) continue;
         epilogue<EPI>(p, sm, tile, item, tid);
         named_bar_sync(1, kConsumers);
     }
+    if (tr && tid == 0) tr[3] = trace_clock();
 }
 
 template <int EPI>

@@ -10,7 +10,7 @@
 namespace sv {
 namespace gemm_core {
 
-constexpr int kStages = 11;  // 176 KB of weights in flight per SM
+constexpr int kStages = 10;  // 160 KB of weights in flight per SM
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 32;
@@ -27,13 +27,15 @@ struct Item {
 
 struct __align__(128) GemmSmem {
     uint8_t w[kStages][kStageWBytes];
-    uint8_t x[kStages][kStageXBytes];
+    uint8_t x[kStages][kStageX32Bytes];
     float cs[kTileRows * kCsLd];
     uint64_t full[kStages];
     uint64_t empty[kStages];
-    float rstd[kMaxBlock];
+    float rstd[kMaxBlock];     // applied in the epilogue (bf16 operands)
+    float rstd_op[kMaxBlock];  // applied to fp32 operands before rounding
     int slots[kMaxContrib];
     int flag;
+    int pos0;                  // cache length at the pass's start (first new position)
     int n_items;
     Item items[kMaxItems];
 };
@@ -131,8 +133,28 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
     if constexpr (EPI == EPI_QKV) {
         const int hd = p.head_dim, half = hd >> 1;
         const int Nq = p.n_heads * hd, Nk = p.n_kv_heads * hd;
-        const int pos0 = p.st->len[p.which];
-        for (int job = tid; job < 64 * p.n; job += kConsumers) {
+        const int pos0 = sm.pos0;
+        constexpr int kJobs = 64 * kMaxBlock / kConsumers;  // rotation pairs per thread, at most
+        // all global loads (rotation, page) first: one round trip, then the stores
+        float2 cn[kJobs];
+        int page[kJobs];
+#pragma unroll
+        for (int u = 0; u < kJobs; ++u) {
+            const int job = tid + u * kConsumers;
+            cn[u] = make_float2(1.f, 0.f);
+            page[u] = 0;
+            if (job >= 64 * p.n) continue;
+            const int j = job >> 6, pr = job & 63;
+            const int hl = pr / half, i = pr - hl * half;
+            const int R = tile * kTileRows + hl * hd + i;
+            const int pos = pos0 + j;
+            if (R < p.N && R < Nq + Nk) cn[u] = p.rope[(size_t)pos * half + i];
+            if (R < p.N && R >= Nq) page[u] = p.block_table[pos / kPageSize];
+        }
+#pragma unroll
+        for (int u = 0; u < kJobs; ++u) {
+            const int job = tid + u * kConsumers;
+            if (job >= 64 * p.n) continue;
             const int j = job >> 6, pr = job & 63;
             const int hl = pr / half, i = pr - hl * half;
             const int ra = hl * hd + i, rb = ra + half;
@@ -142,9 +164,8 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             float va = cs[ra * kCsLd + j] * rs, vb = cs[rb * kCsLd + j] * rs;
             const int pos = pos0 + j;
             if (R < Nq + Nk) {
-                const float2 cn = p.rope[(size_t)pos * half + i];
-                const float na = va * cn.x - vb * cn.y;
-                const float nb = vb * cn.x + va * cn.y;
+                const float na = va * cn[u].x - vb * cn[u].y;
+                const float nb = vb * cn[u].x + va * cn[u].y;
                 va = na;
                 vb = nb;
             }
@@ -155,8 +176,9 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             } else {
                 const bool isk = R < Nq + Nk;
                 const int kvh = (R - (isk ? Nq : Nq + Nk)) / hd;
-                const int page = p.block_table[pos / kPageSize], slot = pos % kPageSize;
-                uint16_t* base = (isk ? p.kpool : p.vpool) + ((size_t)(page * p.n_kv_heads + kvh) * kPageSize) * hd;
+                const int slot = pos % kPageSize;
+                uint16_t* base =
+                    (isk ? p.kpool : p.vpool) + ((size_t)(page[u] * p.n_kv_heads + kvh) * kPageSize) * hd;
                 base[kv_swz(slot, i, hd)] = f2bf(va);
                 base[kv_swz(slot, i + half, hd)] = f2bf(vb);
             }
@@ -167,16 +189,20 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
         if (j < p.n) {
             const int R0 = tile * kTileRows + rg * 8;
             float* xr = p.x + (size_t)j * p.d + R0;
-            float4 x0 = *reinterpret_cast<float4*>(xr);
-            float4 x1 = *reinterpret_cast<float4*>(xr + 4);
+            // every load first (one round trip), then the stores
+            const float4 x0 = *reinterpret_cast<const float4*>(xr);
+            const float4 x1 = *reinterpret_cast<const float4*>(xr + 4);
+            const uint4 gq = *reinterpret_cast<const uint4*>(p.g_next + R0);   // 8 bf16 gains
+            const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
             float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 v[e] += cs[(rg * 8 + e) * kCsLd + j];
                 ssum += v[e] * v[e];
                 const int R = R0 + e;
-                *reinterpret_cast<uint16_t*>(p.xf_out + (size_t)(R >> 6) * kStageXBytes + xfrag_offset(j, R & 63)) =
-                    f2bf(v[e] * bf2f(p.g_next[R]));
+                const float g = __uint_as_float((e & 1) ? (gw[e >> 1] & 0xFFFF0000u) : (gw[e >> 1] << 16));
+                *reinterpret_cast<float*>(p.xf_out + (size_t)(R >> 6) * kStageX32Bytes + xfrag32_offset(j, R & 63)) =
+                    v[e] * g;
             }
             *reinterpret_cast<float4*>(xr) = make_float4(v[0], v[1], v[2], v[3]);
             *reinterpret_cast<float4*>(xr + 4) = make_float4(v[4], v[5], v[6], v[7]);
@@ -312,8 +338,8 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
 
 
 // Accumulators of one tile segment -> shared fp32 tile; for a tile split
-// between CTAs (stream-K), publish the partial and let the last contributor
-// sum all partials in contributor order.  Returns true when this CTA holds
+// between CTAs (stream-K), the other contributors publish their partials and
+// the first contributor sums all partials in contributor order.  Returns true when this CTA holds
 // the complete tile (and must run the epilogue), false otherwise.
 __device__ __forceinline__ bool finish_tile(const GemmParams& p, GemmSmem& sm, int tile, int b0, int b1,
                                             const float (&acc0)[4], const float (&acc1)[4], int tid) {
@@ -415,6 +441,7 @@ __device__ __forceinline__ void compute_rstd(const GemmParams& p, GemmSmem& sm, 
     const int tiles = p.ss_in_tiles;
     const bool norm = p.norm_dim > 0;
     float* buf = sm.cs;
+    if (tid == 0) sm.pos0 = p.st->len[p.which];
     if (norm) {
         const int total = p.n * tiles;  // <= 16 * 64 (d <= 8192)
         for (int i = tid; i < total && i < kTileRows * kCsLd; i += kConsumers) buf[i] = p.ss_in[i];
@@ -427,9 +454,64 @@ __device__ __forceinline__ void compute_rstd(const GemmParams& p, GemmSmem& sm, 
             for (int t = 0; t < tiles; ++t) s += buf[tid * tiles + t];
             r = rsqrtf(s / (float)p.norm_dim + p.norm_eps);
         }
-        sm.rstd[tid] = r;
+        if (p.x_f32) {
+            sm.rstd_op[tid] = r;
+            sm.rstd[tid] = 1.f;
+        } else {
+            sm.rstd_op[tid] = 1.f;
+            sm.rstd[tid] = r;
+        }
     }
     named_bar_sync(1, kConsumers);
+}
+
+// One ring stage of the MMA main loop: warp `warp` multiplies its 16 weight
+// rows by the stage's operand (one or two n8 token tiles).  fp32 operands are
+// scaled by rstd and rounded to bf16 here, which is where the normalisation's
+// rounding happens.
+//
+// The four k16 products of a stage start from zero and the stage sum is added
+// to the running accumulator with an ordinary round-to-nearest fp32 add.  The
+// tensor core's own accumulation does not round to nearest; chaining every k16
+// step into the running sum applies its rounding at the magnitude of the whole
+// dot product once per 16 terms.  On a one-layer model of width 2560 that put
+// the logits about 5x further from fp64-accumulated results than this split.
+__device__ __forceinline__ void mma_stage(const GemmSmem& sm, int s, int warp, int lane, bool two, bool f32,
+                                          float ra0, float ra1, float (&run0)[4], float (&run1)[4]) {
+    const uint8_t* ws = sm.w[s] + warp * 2048 + lane * 16;
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (f32) {
+        const uint8_t* xs = sm.x[s] + lane * 16;
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16) {
+            const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
+            const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
+            const float4 v = *reinterpret_cast<const float4*>(xs + k16 * 512);
+            mma_bf16_16816(acc0, a, pack_bf16x2(v.x * ra0, v.y * ra0), pack_bf16x2(v.z * ra0, v.w * ra0));
+            if (two) {
+                const float4 w = *reinterpret_cast<const float4*>(xs + 2048 + k16 * 512);
+                mma_bf16_16816(acc1, a, pack_bf16x2(w.x * ra1, w.y * ra1), pack_bf16x2(w.z * ra1, w.w * ra1));
+            }
+        }
+    } else {
+        const uint8_t* xs = sm.x[s] + lane * 8;
+#pragma unroll
+        for (int k16 = 0; k16 < 4; ++k16) {
+            const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
+            const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
+            const uint2 bv = *reinterpret_cast<const uint2*>(xs + k16 * 256);
+            mma_bf16_16816(acc0, a, bv.x, bv.y);
+            if (two) {
+                const uint2 bw = *reinterpret_cast<const uint2*>(xs + 1024 + k16 * 256);
+                mma_bf16_16816(acc1, a, bw.x, bw.y);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        run0[i] += acc0[i];
+        run1[i] += acc1[i];
+    }
 }
 
 // Runtime dispatch of the epilogue kinds (the persistent pass kernel runs

@@ -25,6 +25,20 @@ enum EpiKind : int {
 
 // A weight matrix [N][K] repacked as tiles of 128 rows x 64 k in the order the
 // consumer warps read A fragments: [tile][kblock][m16 (8)][k16 (4)][lane][8 bf16].
+// Launch tracing: a traced launch gets kTraceCtas x 4 slots; CTA c writes
+// global-timer stamps at trace[c*4 + k]: k = 0 entry, 1 inputs ready (after
+// the dependency wait), 2 main work done, 3 exit (0 where a kernel has no such
+// point).
+constexpr int kTraceCtas = 512;
+// Kind codes of traced launches other than GEMMs (GEMMs report their EPI_* kind).
+constexpr int kTraceAttnPartial = 16, kTraceAttnCombine = 17, kTraceEmbed = 18, kTraceAccept = 19;
+
+__device__ __forceinline__ long long trace_clock() {
+    long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
 struct PackedMat {
     uint8_t* p = nullptr;
     int N = 0, K = 0, T = 0, KBs = 0;
@@ -35,7 +49,8 @@ struct GemmParams {
     const uint8_t* W;          // packed weights (items mode: expert e at W + e*w_item_stride)
     long long w_item_stride;
     int T, KBs, N;
-    const uint8_t* X;          // fragment-ordered operand [KBs][2 KB] (items: + item*x_item_stride)
+    const uint8_t* X;          // fragment-ordered operand [KBs][2 KB bf16 | 4 KB fp32] (items: + item*x_item_stride)
+    int x_f32;                 // operand holds fp32 x*gain; rstd is applied and bf16 rounding done on read
     long long x_item_stride;
     int n;                     // tokens (1..16)
     int items_mode;            // 0: stream-K over T*KBs; 1: (item, tile) units
@@ -78,6 +93,7 @@ struct GemmParams {
     float* y_store;            // [16][N] (EPI_STORE)
     uint8_t* xe;               // expert-down operands [item][KBs_down][2 KB]
     long long xe_stride;
+    long long* trace;          // optional: this launch's [kTraceCtas][4] stamps (see kTraceCtas)
 };
 
 struct AttnParams {
@@ -91,6 +107,7 @@ struct AttnParams {
     DevState* st;
     int which, n, n_heads, n_kv_heads, head_dim, nch;
     float scale_log2;          // log2(e) / sqrt(hd)
+    long long* trace;          // optional stamps of the partial kernel, then of the combine kernel
 };
 
 // Launchers (stream, PDL).  Return cudaSuccess or the launch error.

@@ -24,7 +24,8 @@ cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaSt
 }
 
 // Writes row j's 8 values starting at R0 into the residual, the next GEMM's
-// operand (x * gain, bf16, fragment order) and returns their sum of squares.
+// operand (x * gain, fp32, fragment order; the consumer applies rstd and
+// rounds) and returns their sum of squares.
 __device__ __forceinline__ float store_residual8(float* xr, const float (&v)[8], int j, int R0, const uint16_t* g_next,
                                                  uint8_t* xf_out) {
     float ssum = 0.f;
@@ -32,8 +33,8 @@ __device__ __forceinline__ float store_residual8(float* xr, const float (&v)[8],
     for (int e = 0; e < 8; ++e) {
         ssum += v[e] * v[e];
         const int R = R0 + e;
-        *reinterpret_cast<uint16_t*>(xf_out + (size_t)(R >> 6) * kStageXBytes + xfrag_offset(j, R & 63)) =
-            f2bf(v[e] * bf2f(g_next[R]));
+        *reinterpret_cast<float*>(xf_out + (size_t)(R >> 6) * kStageX32Bytes + xfrag32_offset(j, R & 63)) =
+            v[e] * bf2f(g_next[R]);
     }
     *reinterpret_cast<float4*>(xr) = make_float4(v[0], v[1], v[2], v[3]);
     *reinterpret_cast<float4*>(xr + 4) = make_float4(v[4], v[5], v[6], v[7]);
@@ -43,8 +44,8 @@ __device__ __forceinline__ float store_residual8(float* xr, const float (&v)[8],
 // x[j] = embed[token_j] (bf16 -> fp32); one CTA per 128 columns, 16 threads
 // per token each owning 8 columns.
 __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ EmbedParams p) {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     const int tile = blockIdx.x, tid = threadIdx.x;
     const int j = tid >> 4, rg = tid & 15;
     float ssum = 0.f;
@@ -70,8 +71,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
 // MoE layer output: x[j] += sum_s gate[j][s] * y_slot[j][s] + y_shared[j],
 // slots in rank order, then the next norm's operand and sum-of-squares.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant__ CombineParams p) {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     const int tile = blockIdx.x, tid = threadIdx.x;
     const int j = tid >> 4, rg = tid & 15;
     float ssum = 0.f;
@@ -120,8 +121,8 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant_
 // the greedy accept rule and the cache-length bookkeeping.
 __global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ AcceptParams p) {
     __shared__ int am[kMaxBlock];
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < p.n) {
         float best = -INFINITY;
@@ -176,14 +177,14 @@ __global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ Acc
 }
 
 __global__ void advance_kernel(DevState* st, int which, int n) {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     st->len[which] += n;
 }
 
 __global__ void rollback_kernel(DevState* st, int which, int new_len) {
-    pdl_launch_dependents();
     pdl_wait();
+    pdl_launch_dependents();
     if (new_len >= 0) {
         st->len[which] = new_len;
     } else if (which == 0) {

@@ -142,8 +142,8 @@ __device__ void embed_phase(const EmbedParams& e, const int* tokens, int tid) {
                 v[q] = bf2f(b[q]);
                 ssum += v[q] * v[q];
                 const int R = R0 + q;
-                *reinterpret_cast<uint16_t*>(e.xf_out + (size_t)(R >> 6) * kStageXBytes + xfrag_offset(j, R & 63)) =
-                    f2bf(v[q] * bf2f(e.g_next[R]));
+                *reinterpret_cast<float*>(e.xf_out + (size_t)(R >> 6) * kStageX32Bytes + xfrag32_offset(j, R & 63)) =
+                    v[q] * bf2f(e.g_next[R]);
             }
             float* xr = e.x + (size_t)j * e.d + R0;
             *reinterpret_cast<float4*>(xr) = make_float4(v[0], v[1], v[2], v[3]);
@@ -162,25 +162,15 @@ __device__ void gemm_phase(const GemmParams& gp, PassSmem& sm, int& q, bool& abo
     StageIter it;
     it.init(gp, 0);
     const bool two = gp.n > 8;
+    const bool f32 = gp.x_f32 != 0;
+    const float ra0 = sm.g.rstd_op[lane >> 2], ra1 = sm.g.rstd_op[8 + (lane >> 2)];
     while (it.valid) {
         const int tile = it.tile, b0 = it.b, b1 = it.b1;
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
         for (int b = b0; b < b1; ++b, ++q) {
             const int s = q % kStages;
             if (!aborted && !mbar_wait(&sm.g.full[s], (q / kStages) & 1, err, 1)) aborted = true;
-            const uint8_t* ws = sm.g.w[s] + warp * 2048 + lane * 16;
-            const uint8_t* xs = sm.g.x[s] + lane * 8;
-#pragma unroll
-            for (int k16 = 0; k16 < 4; ++k16) {
-                const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
-                const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-                const uint2 bv = *reinterpret_cast<const uint2*>(xs + k16 * 256);
-                mma_bf16_16816(acc0, a, bv.x, bv.y);
-                if (two) {
-                    const uint2 bw = *reinterpret_cast<const uint2*>(xs + 1024 + k16 * 256);
-                    mma_bf16_16816(acc1, a, bw.x, bw.y);
-                }
-            }
+            mma_stage(sm.g, s, warp, lane, two, f32, ra0, ra1, acc0, acc1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.g.empty[s]);
         }
@@ -307,7 +297,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) pass_kernel(const __grid_cons
                 const PhaseDesc& D = P.phases[ph];
                 PhaseIter it;
                 it.init(D, nc);
-                const uint32_t xb = P.n > 8 ? (uint32_t)kStageXBytes : (uint32_t)(kStageXBytes / 2);
+                const uint32_t xb = x_stage_bytes(P.n, D.g.x_f32);
                 const uint32_t slab = (uint32_t)(kPageSize * D.a.head_dim * 2);
                 while (it.valid) {
                     const int s = q % kStages;
@@ -347,14 +337,15 @@ __global__ void __launch_bounds__(kPassThreads, 1) pass_kernel(const __grid_cons
                 if (!it.valid) continue;
                 wait_smem_ge(&sm.phase_ok, ph, err, 5);
                 fence_proxy_async();
-                const uint32_t xb = P.n > 8 ? (uint32_t)kStageXBytes : (uint32_t)(kStageXBytes / 2);
+                const uint32_t xb = x_stage_bytes(P.n, D.g.x_f32);
+                const long long xstride = x_kblock_stride(D.g.x_f32);
                 const int hd = D.a.head_dim;
                 const uint32_t slab = (uint32_t)(kPageSize * hd * 2);
                 while (it.valid) {
                     wait_smem_ge(&sm.w_issued, q + 1, err, 6);
                     const int s = q % kStages;
                     if (D.kind == PH_GEMM) {
-                        bulk_g2s(sm.g.x[s], D.g.X + (long long)it.gi.b * kStageXBytes, xb, &sm.g.full[s]);
+                        bulk_g2s(sm.g.x[s], D.g.X + (long long)it.gi.b * xstride, xb, &sm.g.full[s]);
                     } else {
                         const int h = it.u / nc, c = it.u % nc;
                         if ((c + 1) * kAttnChunk > pos0) {  // holds this pass's new keys

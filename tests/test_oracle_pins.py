@@ -159,6 +159,68 @@ def test_attention_closed_forms():
         assert np.max(np.abs(out[h * hd:(h + 1) * hd] - ref)) <= 2 ** -8 * np.max(np.abs(ref)) + 1e-6
 
 
+
+# ----------------------------------------------------------------------------
+# The fp64-accumulation build (same definition, long sums in fp64)
+# ----------------------------------------------------------------------------
+def test_acc64_gemm_is_the_correctly_rounded_dot_product():
+    """bf16 x fp32 products are exact in fp64 and a 300-term fp64 sum is
+    far inside half an fp32 ulp, so each output is float64 BLAS rounded to
+    fp32 (a different result would mean a dropped or misplaced term)."""
+    rng = np.random.default_rng(10)
+    W = synth.normal_bf16((41, 300), 9, 2)
+    X = bf16_np(rng.standard_normal((6, 300))).astype(np.float32)
+    Y = oracle.gemm(W, X, acc64=True)
+    ref = (X.astype(np.float64) @ widen(W).T).astype(np.float32)
+    ulp = np.spacing(np.abs(ref))
+    assert np.all(np.abs(Y.astype(np.float64) - ref) <= ulp)
+    assert np.mean(Y == ref) > 0.99
+    # and it is at least as close to float64 as the fp32 build
+    y32 = oracle.gemm(W, X)
+    exact = X.astype(np.float64) @ widen(W).T
+    assert np.abs(Y - exact).sum() <= np.abs(y32 - exact).sum()
+
+
+def test_acc64_rmsnorm_and_attention_against_float64():
+    d, eps = 2560, 1e-6
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal(d) * 3
+    g = synth.normal_bf16((d,), 5, 3)
+    h = oracle.rmsnorm(x, g, eps, acc64=True)
+    x32 = x.astype(np.float32).astype(np.float64)
+    rstd = np.float32(1.0 / np.sqrt(np.mean(x32 * x32) + eps))
+    ref = bf16_np(x32.astype(np.float32) * rstd * widen(g).astype(np.float32))
+    assert np.mean(h == ref) > 0.999
+    assert np.max(np.abs(h - ref)) <= 2 ** -7 * np.max(np.abs(ref))
+    Hq, Hkv, hd, nk = 4, 1, 128, 2048
+    q = bf16_np(rng.standard_normal(Hq * hd)).astype(np.float32)
+    K = bf16_np(rng.standard_normal((nk, Hkv * hd))).astype(np.float32)
+    V = bf16_np(rng.standard_normal((nk, Hkv * hd))).astype(np.float32)
+    out = oracle.attend(q, K, V, Hq, Hkv, hd, acc64=True)
+    for hh in range(Hq):
+        s = K.astype(np.float64) @ q[hh * hd:(hh + 1) * hd] / math.sqrt(hd)
+        p = np.exp(s - s.max())
+        ref = bf16_np(p @ V.astype(np.float64) / p.sum())
+        got = out[hh * hd:(hh + 1) * hd]
+        assert np.max(np.abs(got - ref)) <= 2 ** -8 * np.max(np.abs(ref)) + 1e-6
+        assert np.mean(got == ref) > 0.95
+
+
+def test_acc64_build_keeps_the_lossless_invariant(tiny_prompt):
+    """Self-speculation equals greedy decoding in the fp64-accumulation build
+    too (MLX self-speculation post), and the two builds agree on a shallow
+    model to well inside the logit tolerance."""
+    cfg = synth.tiny()
+    w = synth.make_weights(cfg)
+    o64 = oracle.Oracle(cfg, w, acc64=True)
+    ref = oracle.greedy_generate(o64, tiny_prompt, 24)
+    out, _ = oracle.selfspec_generate(o64, oracle.layer_skip_plan(cfg.n_layers, 0.3), tiny_prompt, 24, 4)
+    assert out == ref
+    o32 = oracle.Oracle(cfg, w)
+    a, _, _ = o32.forward(o32.new_cache(), o32.full_plan, tiny_prompt, 0)
+    b, _, _ = o64.forward(o64.new_cache(), o64.full_plan, tiny_prompt, 0)
+    assert np.max(np.abs(a - b)) < 2e-2
+
 def test_router_topk_against_sort():
     rng = np.random.default_rng(4)
     for trial in range(200):
@@ -381,5 +443,17 @@ def test_moe_per_token_routing_recorded():
             assert np.all(np.diff(gates[l, t]) <= 0)   # ranked by probability
     # forcing the computed routing reproduces the logits bitwise
     c2 = orc.new_cache()
-    lg2, ids2, _ = orc.forward(c2, orc.full_plan, p, 0, want_routing=True, forced_ids=np.maximum(ids, 0))
+    probs = np.zeros((cfg.n_layers, 12, cfg.n_experts), np.float32)
+    lg2, ids2, gates2 = orc.forward(c2, orc.full_plan, p, 0, want_routing=True, forced_ids=np.maximum(ids, 0),
+                                    probs=probs)
     assert np.array_equal(lg, lg2)
+    # the reported router probabilities: a distribution whose top-k (lowest id
+    # first on ties) is the free choice, with the gates read off it
+    assert np.all(probs[0] == 0)
+    for l in range(1, cfg.n_layers):
+        for t in range(12):
+            pr = probs[l, t].astype(np.float64)
+            assert abs(pr.sum() - 1.0) < 1e-5 and np.all(pr > 0)
+            top = sorted(range(cfg.n_experts), key=lambda e: (-pr[e], e))[:cfg.top_k]
+            assert list(ids[l, t]) == top
+            assert np.array_equal(gates2[l, t], probs[l, t][ids[l, t]])
