@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kConsumerWarps);
+            mbar_init(&sm.ready[s], 1);
         }
         fence_barrier_init();
     }
@@ -69,6 +70,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int n_items = p.items_mode ? sm.n_items : 0;
     const uint32_t xb = x_stage_bytes(p.n, p.x_f32);
     const long long xstride = x_kblock_stride(p.x_f32);
+
+    if (warp == kConsumerWarps + 1) {
+        // ------- converter: fp32 operand stages -> bf16 fragments, once per stage -------
+        if (!p.x_f32) return;
+        named_bar_sync(2, kConsumers + 32);   // the consumers' rstd is in shared memory
+        const bool two = p.n > 8;
+        StageIter it;
+        it.init(p, n_items);
+        bool aborted = false;
+        for (int q = 0; it.valid; ++q) {
+            const int s = q % kStages;
+            if (!aborted && !mbar_wait(&sm.full[s], (q / kStages) & 1, err, 4)) aborted = true;
+            convert_stage(sm.x[s], two, sm.rstd_op, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.ready[s]);
+            it.advance();
+        }
+        return;
+    }
 
     if (warp == kConsumerWarps) {
         // ---------------- producer: one lane issues every bulk copy ----------------
@@ -122,13 +142,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         pdl_launch_dependents();
     }
     compute_rstd(p, sm, tid);
+    if (p.x_f32) named_bar_arrive(2, kConsumers + 32);   // release the converter
     if (tr && tid == 0) tr[1] = trace_clock();
 
     StageIter it;
     it.init(p, n_items);
     const bool two = p.n > 8;
-    const bool f32 = p.x_f32 != 0;
-    const float ra0 = sm.rstd_op[lane >> 2], ra1 = sm.rstd_op[8 + (lane >> 2)];
+    // fp32 operands reach the consumers already converted (ready barrier)
+    uint64_t* gate = p.x_f32 ? sm.ready : sm.full;
     int q = 0;
     bool aborted = false;
 
@@ -137,8 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
         for (int b = b0; b < b1; ++b, ++q) {
             const int s = q % kStages;
-            if (!aborted && !mbar_wait(&sm.full[s], (q / kStages) & 1, err, 1)) aborted = true;
-            mma_stage(sm, s, warp, lane, two, f32, ra0, ra1, acc0, acc1);
+            if (!aborted && !mbar_wait(&gate[s], (q / kStages) & 1, err, 1)) aborted = true;
+            mma_stage(sm, s, warp, lane, two, false, 1.f, 1.f, acc0, acc1);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.empty[s]);
         }

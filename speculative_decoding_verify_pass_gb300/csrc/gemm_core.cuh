@@ -13,7 +13,7 @@ namespace gemm_core {
 constexpr int kStages = 10;  // 160 KB of weights in flight per SM
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;
+constexpr int kThreads = kConsumers + 64;  // + one producer warp + one operand-converter warp
 constexpr int kCsLd = 20;  // padded row stride of the fp32 tile
 constexpr int kMaxItems = kMaxBlock * kMaxTopK;
 constexpr int kPartFloats = kTileRows * kMaxBlock;
@@ -31,6 +31,7 @@ struct __align__(128) GemmSmem {
     float cs[kTileRows * kCsLd];
     uint64_t full[kStages];
     uint64_t empty[kStages];
+    uint64_t ready[kStages];   // fp32 operand stage converted to bf16 fragments in place
     float rstd[kMaxBlock];     // applied in the epilogue (bf16 operands)
     float rstd_op[kMaxBlock];  // applied to fp32 operands before rounding
     int slots[kMaxContrib];
@@ -511,6 +512,30 @@ __device__ __forceinline__ void mma_stage(const GemmSmem& sm, int s, int warp, i
     for (int i = 0; i < 4; ++i) {
         run0[i] += acc0[i];
         run1[i] += acc1[i];
+    }
+}
+
+// Converts one ring stage's fp32 operand (x*gain, fp32 fragment order) in
+// place into bf16 B fragments of x*gain*rstd (the layout bf16 operands use),
+// by one warp: each lane reads its entries for every (n8, k16) first, then
+// writes, so the half-size output cannot overwrite unread input.  The
+// rounding is the one the consumers would otherwise do: fp32 product, then
+// bf16 round-to-nearest-even.
+__device__ __forceinline__ void convert_stage(uint8_t* xs, bool two, const float* rstd_op, int lane) {
+    float4 v[8];
+    const int entries = two ? 8 : 4;   // (n8, k16) pairs
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+        if (t < entries) v[t] = *reinterpret_cast<const float4*>(xs + (t * 32 + lane) * 16);
+    __syncwarp();
+    const float r0 = rstd_op[lane >> 2], r1 = rstd_op[8 + (lane >> 2)];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+        if (t < entries) {
+            const float r = t < 4 ? r0 : r1;
+            *reinterpret_cast<uint2*>(xs + (t * 32 + lane) * 8) =
+                make_uint2(pack_bf16x2(v[t].x * r, v[t].y * r), pack_bf16x2(v[t].z * r, v[t].w * r));
+        }
     }
 }
 
