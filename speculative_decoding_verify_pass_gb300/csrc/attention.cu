@@ -13,7 +13,7 @@
 //    on bf16 tensor-core MMA with fp32 accumulation, P as a bf16 high part
 //    plus a bf16 low part;
 //  * the two pages of a row group merge in shared memory and the CTA writes
-//    one (row max, row sum, unnormalised O) per row; a merge kernel (one CTA
+//    one (row max, row sum, unnormalised O) per row; a merge kernel (one warp
 //    per query head and token) combines the chunks in increasing order.
 // Chunk boundaries are absolute positions, so a query's result does not
 // depend on the block size n; chunks entirely past a query's last key
@@ -81,9 +81,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const __grid
     if (tr) tr[3] = trace_clock();
 }
 
-// One CTA per (query head, token): the page partials merged in page order.
+// Two rows (query head, token) per CTA, one warp each: the chunk partials
+// of a row merged in chunk order.
+template <int HD>
 __global__ void __launch_bounds__(attn_core::kAttnCombThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
-    __shared__ float red[3 * attn_core::kMaxChunks];
     long long* tr = (p.trace && blockIdx.x < kTraceCtas && threadIdx.x == 0)
                         ? p.trace + (size_t)(kTraceCtas + blockIdx.x) * 4 : nullptr;
     if (tr) tr[0] = trace_clock();
@@ -93,7 +94,8 @@ __global__ void __launch_bounds__(attn_core::kAttnCombThreads) attn_combine_kern
     const int total = p.st->len[p.which] + p.n;
     int nc = (total + kAttnChunk - 1) / kAttnChunk;
     if (nc > p.nch) nc = p.nch;
-    attn_core::comb_units(p, red, threadIdx.x, nc, blockIdx.x, gridDim.x);
+    constexpr int kWarps = attn_core::kAttnCombThreads / 32;
+    attn_core::comb_rows<HD>(p, blockIdx.x * kWarps + (threadIdx.x >> 5), gridDim.x * kWarps, threadIdx.x & 31, nc);
     if (tr) tr[3] = trace_clock();
 }
 
@@ -126,7 +128,7 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl) {
     AttnParams q = p;
     void* args[] = {&q};
     cudaError_t e;
-    const dim3 g1((unsigned)p.n_kv_heads, (unsigned)p.nch), g2((unsigned)(p.n_heads * p.n));
+    const dim3 g1((unsigned)p.n_kv_heads, (unsigned)p.nch), g2((unsigned)((p.n_heads * p.n + attn_core::kAttnCombThreads / 32 - 1) / (attn_core::kAttnCombThreads / 32)));
     if (p.head_dim == 128)
         e = launch_pdl((const void*)attn_partial_kernel<128>, g1, dim3(kAttnThreads), 2 * kAttnChunk * 128 * 2, s, pdl,
                        args);
@@ -136,7 +138,8 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl) {
     else
         return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;
-    return launch_pdl((const void*)attn_combine_kernel, g2, dim3(attn_core::kAttnCombThreads), 0, s, pdl, args);
+    const void* comb = p.head_dim == 128 ? (const void*)attn_combine_kernel<128> : (const void*)attn_combine_kernel<64>;
+    return launch_pdl(comb, g2, dim3(attn_core::kAttnCombThreads), 0, s, pdl, args);
 }
 
 }  // namespace sv

@@ -20,8 +20,7 @@ namespace sv {
 namespace attn_core {
 
 constexpr int kAttnUnitThreads = 256;  // 8 warps (named barrier 1)
-constexpr int kAttnCombThreads = 256;
-constexpr int kMaxChunks = 512;        // 65536 positions / 128
+constexpr int kAttnCombThreads = 64;   // merge kernel: 2 warps, one merged row each
 
 // One warp's 16 rows (row group rg) against one 64-key page slab (keys
 // key0..key0+63 in absolute positions).  Outputs stay in registers.
@@ -188,63 +187,87 @@ __device__ __forceinline__ void attn_unit(const AttnParams& a, uint16_t* sk0, ui
     }
 }
 
-// Units (query head, token) u0, u0+ustep, ...: merge the nc chunk partials of
-// the row in chunk order and write the bf16 output into the O projection's
-// operand.  All 256 threads (named barrier 1); smem needs 3*kMaxChunks floats.
-__device__ __forceinline__ void comb_units(const AttnParams& a, float* smem, int tid, int nc, int u0, int ustep) {
+// Rows (query head, token) u0, u0+ustep, ...: one warp per row merges the nc
+// chunk partials in chunk order and writes the bf16 output into the O
+// projection's operand.  Each lane owns HD/32 consecutive dimensions.  The
+// first kFirst chunks' partial outputs are loaded together with the chunk
+// statistics (their addresses do not depend on them), so a row of up to
+// kFirst chunks costs one round trip to L2.  Every lane reads every chunk's
+// (max, sum) (uniform loads) and forms the same weights; the sums run in
+// chunk order, so a row's result does not depend on the block size.
+template <int HD>
+__device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep, int lane, int nc) {
+    constexpr int V = HD / 32;   // dimensions per lane: 4 (hd 128) or 2 (hd 64)
+    constexpr int kFirst = 24;
     const int G = a.n_heads / a.n_kv_heads;
-    const int HD = a.head_dim;
     const int U = a.n_heads * a.n;
-    const int groups = kAttnCombThreads / HD;  // chunk groups: 2 (hd 128) or 4 (hd 64)
-    const int dim = tid % HD, grp = tid / HD;
-    float* ms = smem;                         // [kMaxChunks] chunk maxima
-    float* ws = smem + kMaxChunks;            // [kMaxChunks] merge weights
-    float* red = smem + 2 * kMaxChunks;       // [kAttnCombThreads]
+    const size_t cstride = (size_t)64 * HD;
     for (int u = u0; u < U; u += ustep) {
         const int qh = u % a.n_heads, j = u / a.n_heads;
         const int h = qh / G, r = j * G + qh % G;
         const float2* ml = a.part_ml + (size_t)h * a.nch * 64 + r;
-        // all chunk statistics in one sweep
-        for (int c = tid; c < nc; c += kAttnCombThreads) {
-            const float2 v = ml[(size_t)c * 64];
-            ms[c] = v.x;
-            ws[c] = v.y;
+        const float* po = a.part_o + ((size_t)h * a.nch * 64 + r) * HD + lane * V;
+        float ob[kFirst][V];
+#pragma unroll
+        for (int t = 0; t < kFirst; ++t) {
+            if (t < nc) {
+                if constexpr (V == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(po + (size_t)t * cstride);
+                    ob[t][0] = v.x; ob[t][1] = v.y; ob[t][2] = v.z; ob[t][3] = v.w;
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(po + (size_t)t * cstride);
+                    ob[t][0] = v.x; ob[t][1] = v.y;
+                }
+            }
         }
-        named_bar_sync(1, kAttnCombThreads);
         float M = -1e30f;
-        for (int c = 0; c < nc; ++c) M = fmaxf(M, ms[c]);
-        float L = 0.f;
-        for (int c = 0; c < nc; ++c) L += exp2f(ms[c] - M) * ws[c];
-        named_bar_sync(1, kAttnCombThreads);
-        for (int c = tid; c < nc; c += kAttnCombThreads) ws[c] = exp2f(ms[c] - M);
-        named_bar_sync(1, kAttnCombThreads);
-        // this thread: dimension dim over chunks grp, grp+groups, ... (16 loads in flight)
-        const float* po = a.part_o + ((size_t)h * a.nch * 64 + r) * HD + dim;
-        const size_t cstride = (size_t)64 * HD;
-        float O = 0.f;
-        for (int c0 = grp; c0 < nc; c0 += 16 * groups) {  // predicated batches: 16 loads in flight
-            float v[16];
+        for (int c0 = 0; c0 < nc; c0 += 8) {   // statistics: eight loads in flight
+            float m[8];
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int c = c0 + t * groups;
-                v[t] = c < nc ? po[(size_t)c * cstride] : 0.f;
-            }
+            for (int t = 0; t < 8; ++t) m[t] = c0 + t < nc ? ml[(size_t)(c0 + t) * 64].x : -1e30f;
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const int c = c0 + t * groups;
-                if (c < nc) O += ws[c] * v[t];
+            for (int t = 0; t < 8; ++t) M = fmaxf(M, m[t]);
+        }
+        float L = 0.f, O[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) O[e] = 0.f;
+#pragma unroll
+        for (int t = 0; t < kFirst; ++t) {
+            if (t < nc) {
+                const float2 st = ml[(size_t)t * 64];
+                const float w = exp2f(st.x - M);
+                L += w * st.y;
+#pragma unroll
+                for (int e = 0; e < V; ++e) O[e] += w * ob[t][e];
             }
         }
-        red[tid] = O;
-        named_bar_sync(1, kAttnCombThreads);
-        if (grp == 0) {
-            float tot = 0.f;
-            for (int gg = 0; gg < groups; ++gg) tot += red[gg * HD + dim];
-            const int k = qh * HD + dim;
-            *reinterpret_cast<uint16_t*>(a.xf_out + (size_t)(k >> 6) * kStageXBytes + xfrag_offset(j, k & 63)) =
-                f2bf(tot / L);
+        for (int c0 = kFirst; c0 < nc; c0 += 8) {   // longer rows: eight chunks in flight
+            float ov[8][V];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (c0 + t < nc) {
+#pragma unroll
+                    for (int e = 0; e < V; ++e) ov[t][e] = po[(size_t)(c0 + t) * cstride + e];
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (c0 + t < nc) {
+                    const float2 st = ml[(size_t)(c0 + t) * 64];
+                    const float w = exp2f(st.x - M);
+                    L += w * st.y;
+#pragma unroll
+                    for (int e = 0; e < V; ++e) O[e] += w * ov[t][e];
+                }
+            }
         }
-        named_bar_sync(1, kAttnCombThreads);
+        const int k = qh * HD + lane * V;
+#pragma unroll
+        for (int e = 0; e < V; e += 2) {
+            const int kk = (k + e) & 63;
+            *reinterpret_cast<uint32_t*>(a.xf_out + (size_t)((k + e) >> 6) * kStageXBytes + xfrag_offset(j, kk)) =
+                pack_bf16x2(O[e] / L, O[e + 1] / L);
+        }
     }
 }
 

@@ -210,7 +210,12 @@ __device__ void attn_phase(const AttnParams& a, PassSmem& sm, int& q, bool& abor
 }
 
 __device__ void comb_phase(const AttnParams& a, PassSmem& sm, int tid, int nc) {
-    attn_core::comb_units(a, sm.g.cs, tid, nc, blockIdx.x, gridDim.x);
+    (void)sm;
+    const int w0 = blockIdx.x * kConsumerWarps + (tid >> 5), ws = gridDim.x * kConsumerWarps;
+    if (a.head_dim == 128)
+        attn_core::comb_rows<128>(a, w0, ws, tid & 31, nc);
+    else
+        attn_core::comb_rows<64>(a, w0, ws, tid & 31, nc);
 }
 
 __device__ void accept_phase(const PassParams& P, PassSmem& sm, int tid, int pos0) {
