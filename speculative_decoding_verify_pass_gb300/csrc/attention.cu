@@ -8,13 +8,13 @@
 //  * both pages' K and V slabs arrive by 1-D bulk copies (they are contiguous
 //    in the page layout, and stored chunk-swizzled so fragment loads are
 //    bank-conflict free);
-//  * 8 warps: 4 groups of 16 of the n*G query rows (G query heads per kv
-//    head, <= 64 rows) times the chunk's 2 pages; S = Q K^T and O = P V run
-//    on bf16 tensor-core MMA with fp32 accumulation, P as a bf16 high part
-//    plus a bf16 low part;
-//  * the two pages of a row group merge in shared memory and the CTA writes
-//    one (row max, row sum, unnormalised O) per row; a merge kernel (one warp
-//    per query head and token) combines the chunks in increasing order.
+//  * the n*G query rows (G query heads per kv head, <= 64 rows) are taken 16
+//    at a time; the 8 warps split S = Q K^T by keys (16 each) and O = P V by
+//    output dimensions (16 each), on bf16 tensor-core MMA with fp32
+//    accumulation, P as a bf16 high part plus a bf16 low part;
+//  * the CTA writes one (row max, row sum, unnormalised O) per row; a merge
+//    kernel (one warp per query head and token) combines the chunks in
+//    increasing order.
 // Chunk boundaries are absolute positions, so a query's result does not
 // depend on the block size n; chunks entirely past a query's last key
 // contribute exactly zero.
@@ -29,7 +29,7 @@ namespace {
 constexpr int kAttnThreads = attn_core::kAttnUnitThreads;  // 8 warps: 4 row groups x 2 pages
 
 template <int HD>
-__global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __maxnreg__(192) attn_partial_kernel(const __grid_constant__ AttnParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint16_t* sk = reinterpret_cast<uint16_t*>(smem_raw);
     uint16_t* svv = sk + kAttnChunk * HD;
@@ -74,10 +74,22 @@ __global__ void __launch_bounds__(kAttnThreads) attn_partial_kernel(const __grid
     if (tid == 0)
         for (int pg = 0; pg < 2; ++pg)
             if (start + (pg + 1) * kPageSize > pos0) issue(pg);   // holds new rows
+    // the unit's query rows into shared memory (one round trip for all row groups)
+    float* scratch = reinterpret_cast<float*>(smem_raw + 2 * kAttnChunk * HD * 2);
+    uint16_t* qs = reinterpret_cast<uint16_t*>(smem_raw + 2 * kAttnChunk * HD * 2 + attn_core::kAttnScratchBytes);
+    const int G = p.n_heads / p.n_kv_heads, R = p.n * G;
+    for (int c = tid; c < R * (HD / 8); c += kAttnThreads) {
+        const int r = c / (HD / 8), q = c % (HD / 8);
+        cp_async16(qs + r * attn_core::q_stride<HD>() + q * 8,
+                   p.qbuf + ((size_t)(r / G) * p.n_heads + h * G + r % G) * HD + q * 8);
+    }
+    cp_async_wait_all();
     __syncthreads();
-    mbar_wait(&bar, 0, &p.st->error, 3);
-    if (tr) tr[2] = trace_clock();
-    attn_core::attn_unit<HD>(p, sk, sk + kPageSize * HD, svv, svv + kPageSize * HD, h, chunk, pos0, tid);
+    attn_core::attn_unit<HD>(p, sk, sk + kPageSize * HD, svv, svv + kPageSize * HD, scratch, qs, 4, h, chunk, pos0, tid,
+                             [&] {
+                                 mbar_wait(&bar, 0, &p.st->error, 3);
+                                 if (tr) tr[2] = trace_clock();
+                             });
     if (tr) tr[3] = trace_clock();
 }
 
@@ -115,13 +127,19 @@ cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaS
 
 }  // namespace
 
+// Slabs + scratch, padded so that two units never share an SM: a unit's
+// slab loads then have a whole SM's share of HBM bandwidth.
+constexpr int attn_smem_used(int hd) {
+    return 2 * kAttnChunk * hd * 2 + attn_core::kAttnScratchBytes + kMaxBlock * 4 * (hd + 8) * 2;  // slabs, scratch, q
+}
+constexpr int attn_smem(int hd) { return attn_smem_used(hd) > 116 * 1024 ? attn_smem_used(hd) : 116 * 1024; }
+
 cudaError_t attention_configure(int device) {
     (void)device;
     cudaError_t e = cudaFuncSetAttribute(attn_partial_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         2 * kAttnChunk * 128 * 2);
+                                         attn_smem(128));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(attn_partial_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                2 * kAttnChunk * 64 * 2);
+    return cudaFuncSetAttribute(attn_partial_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, attn_smem(64));
 }
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl) {
@@ -130,11 +148,9 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl) {
     cudaError_t e;
     const dim3 g1((unsigned)p.n_kv_heads, (unsigned)p.nch), g2((unsigned)((p.n_heads * p.n + attn_core::kAttnCombThreads / 32 - 1) / (attn_core::kAttnCombThreads / 32)));
     if (p.head_dim == 128)
-        e = launch_pdl((const void*)attn_partial_kernel<128>, g1, dim3(kAttnThreads), 2 * kAttnChunk * 128 * 2, s, pdl,
-                       args);
+        e = launch_pdl((const void*)attn_partial_kernel<128>, g1, dim3(kAttnThreads), attn_smem(128), s, pdl, args);
     else if (p.head_dim == 64)
-        e = launch_pdl((const void*)attn_partial_kernel<64>, g1, dim3(kAttnThreads), 2 * kAttnChunk * 64 * 2, s, pdl,
-                       args);
+        e = launch_pdl((const void*)attn_partial_kernel<64>, g1, dim3(kAttnThreads), attn_smem(64), s, pdl, args);
     else
         return cudaErrorInvalidValue;
     if (e != cudaSuccess) return e;

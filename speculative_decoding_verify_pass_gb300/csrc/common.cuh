@@ -153,6 +153,14 @@ __device__ __forceinline__ int ld_acquire_gpu_i32(const int* p) {
     return v;
 }
 
+// Asynchronous 16-byte global -> shared copy (completes at cp_async_wait_all).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 // Bulk prefetch of a global range into L2 (no shared-memory destination, no
 // completion): warms the 129 MB L2 ahead of the TMA loads that will read it.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {

@@ -198,10 +198,12 @@ __device__ void attn_phase(const AttnParams& a, PassSmem& sm, int& q, bool& abor
         uint16_t* k1 = reinterpret_cast<uint16_t*>(sm.g.w[(q + 1) % kStages]);
         uint16_t* v0 = reinterpret_cast<uint16_t*>(sm.g.w[(q + 2) % kStages]);
         uint16_t* v1 = reinterpret_cast<uint16_t*>(sm.g.w[(q + 3) % kStages]);
+        static_assert(attn_core::kAttnSlotBytes <= (int)sizeof(sm.g.cs), "attention scratch must fit the tile buffer");
+        auto ready = [] {};   // the slab stages were waited for above
         if (a.head_dim == 128)
-            attn_core::attn_unit<128>(a, k0, k1, v0, v1, h, c, pos0, tid);
+            attn_core::attn_unit_c<128, 8>(a, k0, k1, v0, v1, sm.g.cs, nullptr, h, c, pos0, tid, ready);
         else
-            attn_core::attn_unit<64>(a, k0, k1, v0, v1, h, c, pos0, tid);
+            attn_core::attn_unit_c<64, 8>(a, k0, k1, v0, v1, sm.g.cs, nullptr, h, c, pos0, tid, ready);
         __syncwarp();
         if (lane == 0)
             for (int t = 0; t < 4; ++t) mbar_arrive(&sm.g.empty[(q + t) % kStages]);
