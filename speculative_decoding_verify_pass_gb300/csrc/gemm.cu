@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (p.items_mode) {  // the work list depends on the router's output
         pdl_wait();
         pdl_launch_dependents();
-        if (tid == 0) build_items(p, sm);
+        build_items(p, sm, tid, kThreads);
         __syncthreads();
     }
     const int n_items = p.items_mode ? sm.n_items : 0;

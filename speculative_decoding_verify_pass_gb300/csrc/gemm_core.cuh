@@ -38,6 +38,7 @@ struct __align__(128) GemmSmem {
     int flag;
     int pos0;                  // cache length at the pass's start (first new position)
     int n_items;
+    int emask[kMaxExperts];    // dedup work list: tokens routed to each expert
     Item items[kMaxItems];
 };
 
@@ -89,37 +90,50 @@ struct StageIter {
     }
 };
 
-__device__ __forceinline__ void build_items(const GemmParams& p, GemmSmem& sm) {
-    const int n = p.n, k = p.top_k;
-    int cnt = 0;
-    if (p.moe_mode == 0) {  // per slot: one item per (token, slot)
-        for (int j = 0; j < n; ++j)
-            for (int s = 0; s < k; ++s) {
-                Item& it = sm.items[cnt++];
-                it.expert = p.route_ids[j * k + s];
-                it.mask = 1 << j;
-                for (int t = 0; t < kMaxBlock; ++t) it.slot[t] = -1;
-                it.slot[j] = (signed char)s;
-            }
-    } else {  // dedup: one item per distinct expert, ascending id
-        unsigned long long used = 0ull;
-        for (int j = 0; j < n; ++j)
-            for (int s = 0; s < k; ++s) used |= 1ull << (p.route_ids[j * k + s] & 63);
-        for (int e = 0; e < kMaxExperts; ++e) {
-            if (!((used >> e) & 1ull)) continue;
-            Item& it = sm.items[cnt++];
-            it.expert = e;
-            it.mask = 0;
+// The expert work list of one launch, built by all `nthreads` threads of the
+// CTA (call before any role split; contains CTA barriers).  Per slot: item
+// j*k + s is token j's s-th expert.  Dedup: one item per distinct expert in
+// ascending id, with the tokens that route to it and their slots.
+__device__ __forceinline__ void build_items(const GemmParams& p, GemmSmem& sm, int tid, int nthreads) {
+    const int n = p.n, k = p.top_k, nk = n * k;
+    int* ids = sm.slots;                  // the block's routing, [n][k] (<= 96 entries)
+    for (int i = tid; i < nk; i += nthreads) ids[i] = p.route_ids[i];
+    __syncthreads();
+    if (p.moe_mode == 0) {
+        for (int i = tid; i < nk; i += nthreads) {
+            const int j = i / k;
+            Item& it = sm.items[i];
+            it.expert = ids[i];
+            it.mask = 1 << j;
             for (int t = 0; t < kMaxBlock; ++t) it.slot[t] = -1;
-            for (int j = 0; j < n; ++j)
-                for (int s = 0; s < k; ++s)
-                    if (p.route_ids[j * k + s] == e) {
-                        it.mask |= 1 << j;
-                        it.slot[j] = (signed char)s;
-                    }
+            it.slot[j] = (signed char)(i % k);
         }
+        if (tid == 0) sm.n_items = nk;
+        return;
     }
-    sm.n_items = cnt;
+    for (int e = tid; e < kMaxExperts; e += nthreads) {   // tokens routed to expert e
+        int mask = 0;
+        for (int i = 0; i < nk; ++i)
+            if ((ids[i] & 63) == e) mask |= 1 << (i / k);
+        sm.emask[e] = mask;
+    }
+    __syncthreads();
+    for (int e = tid; e < kMaxExperts; e += nthreads) {
+        if (!sm.emask[e]) continue;
+        int idx = 0;   // items of smaller experts
+        for (int f = 0; f < e; ++f) idx += sm.emask[f] != 0;
+        Item& it = sm.items[idx];
+        it.expert = e;
+        it.mask = sm.emask[e];
+        for (int t = 0; t < kMaxBlock; ++t) it.slot[t] = -1;
+        for (int i = 0; i < nk; ++i)
+            if ((ids[i] & 63) == e) it.slot[i / k] = (signed char)(i % k);
+    }
+    if (tid == 0) {
+        int cnt = 0;
+        for (int e = 0; e < kMaxExperts; ++e) cnt += sm.emask[e] != 0;
+        sm.n_items = cnt;
+    }
 }
 
 // Stream-K ownership: CTA owning flattened iteration i, and its range start.
