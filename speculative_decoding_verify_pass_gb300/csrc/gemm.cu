@@ -137,6 +137,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 
     // -------------------- consumers: 8 warps, 16 weight rows each --------------------
+    // the cache length is not written by the preceding kernel (trigger rule)
+    if constexpr (EPI == EPI_QKV) {
+        if (tid == 0) sm.pos0 = p.st->len[p.which];   // published by compute_rstd's barriers
+    }
     if (!p.items_mode) {
         pdl_wait();
         pdl_launch_dependents();

@@ -456,7 +456,6 @@ __device__ __forceinline__ void compute_rstd(const GemmParams& p, GemmSmem& sm, 
     const int tiles = p.ss_in_tiles;
     const bool norm = p.norm_dim > 0;
     float* buf = sm.cs;
-    if (tid == 0) sm.pos0 = p.st->len[p.which];
     if (norm) {
         const int total = p.n * tiles;  // <= 16 * 64 (d <= 8192)
         for (int i = tid; i < total && i < kTileRows * kCsLd; i += kConsumers) buf[i] = p.ss_in[i];

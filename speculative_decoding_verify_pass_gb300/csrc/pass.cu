@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(kPassThreads, 1) pass_kernel(const __grid_cons
             for (int i = tid; i < words; i += kConsumers) dstw[i] = srcw[i];
             named_bar_sync(1, kConsumers);
             if (tid == 0 && sm.gp.epi == EPI_LMHEAD) sm.gp.logits = P.logits;
+            if (tid == 0) sm.g.pos0 = pos0;
             compute_rstd(sm.gp, sm.g, tid);
             gemm_phase(sm.gp, sm, q, aborted, tid, err, tr);
         } else if (kind == PH_ATTN) {
