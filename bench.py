@@ -732,6 +732,58 @@ def suite_moe(args):
     m.close()
 
 
+def suite_extras(args):
+    """The tiny config (correctness-size model: greedy vs self-speculative
+    tokens/s at gamma 4 over the middle-two-of-four plan, verify time per
+    pass), the Qwen3-4B prefill of a 2048-token prompt, and plain greedy
+    decoding against the self-speculative cycle on the Qwen3-4B shape."""
+    import numpy as np
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    # tiny: 128-token prompt, 64 tokens, skip layers {1, 2}, gamma 4
+    cfg = synth.tiny()
+    w = synth.make_weights(cfg)
+    m = sv.Model(cfg, w, draft_plan=[0, 3])
+    prompt = synth.prompt(cfg, 128).tolist()
+    for fn, name in ((lambda: m.greedy(prompt, 64), "greedy"), (lambda: m.selfspec(prompt, 64, 4)[0], "selfspec")):
+        fn()
+        torch.cuda.synchronize()
+        t0 = time.time()
+        out = fn()
+        torch.cuda.synchronize()
+        dt = time.time() - t0
+        _emit({"suite": "extras", "what": "tiny_" + name, "tokens": len(out), "wall_s": round(dt, 4),
+               "tok_s_host_loop": round(len(out) / dt, 1)})
+    m.kv_set_len(0, 128)
+    us = _verify_us(torch, sv, m, prompt[:5], 128)
+    _emit({"suite": "extras", "what": "tiny_verify_n5", "ctx": 128, "us": round(us, 1)})
+    m.close()
+    # Qwen3-4B: prefill of 2048 tokens; plain greedy decode vs the self-speculative cycle
+    cfg = synth.qwen3_4b(max_ctx=2048 + 1024)
+    plan = sv.layer_skip_plan(cfg.n_layers, 0.5)
+    w = synth.make_weights(cfg)
+    m = sv.Model(cfg, w, draft_plan=plan)
+    prompt = synth.prompt(cfg, 2048).tolist()
+    m.prefill(prompt)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        m.kv_set_len(0, 0)
+        m.kv_set_len(1, 0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        m.prefill(prompt)
+        e1.record()
+        torch.cuda.synchronize()
+    _emit({"suite": "extras", "what": "qwen3-4b_prefill", "tokens": 2048, "ms": round(e0.elapsed_time(e1), 2),
+           "tok_s": round(2048 / (e0.elapsed_time(e1) / 1e3), 1)})
+    ctx = m.kv_len(0)
+    us1 = _verify_us(torch, sv, m, prompt[:1], ctx)
+    _emit({"suite": "extras", "what": "qwen3-4b_plain_greedy", "ctx": ctx, "us_per_token": round(us1, 1),
+           "tok_s": round(1e6 / us1, 1)})
+    m.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -745,13 +797,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for counter captures; the line names it)")
-    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "moe"],
+    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "moe", "extras"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
     if args.suite:
         import __graft_entry__
         __graft_entry__.build()
-        {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash, "moe": suite_moe}[args.suite](args)
+        {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash, "moe": suite_moe,
+         "extras": suite_extras}[args.suite](args)
         return
     if args.warmup < 3:
         args.warmup = 3
