@@ -746,8 +746,13 @@ def suite_extras(args):
     w = synth.make_weights(cfg)
     m = sv.Model(cfg, w, draft_plan=[0, 3])
     prompt = synth.prompt(cfg, 128).tolist()
+    def reset():
+        m.kv_set_len(0, 0)
+        m.kv_set_len(1, 0)
     for fn, name in ((lambda: m.greedy(prompt, 64), "greedy"), (lambda: m.selfspec(prompt, 64, 4)[0], "selfspec")):
+        reset()
         fn()
+        reset()
         torch.cuda.synchronize()
         t0 = time.time()
         out = fn()
@@ -755,7 +760,8 @@ def suite_extras(args):
         dt = time.time() - t0
         _emit({"suite": "extras", "what": "tiny_" + name, "tokens": len(out), "wall_s": round(dt, 4),
                "tok_s_host_loop": round(len(out) / dt, 1)})
-    m.kv_set_len(0, 128)
+    reset()
+    m.prefill(prompt)
     us = _verify_us(torch, sv, m, prompt[:5], 128)
     _emit({"suite": "extras", "what": "tiny_verify_n5", "ctx": 128, "us": round(us, 1)})
     m.close()
