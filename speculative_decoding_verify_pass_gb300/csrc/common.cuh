@@ -161,11 +161,6 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
 }
 
-// Bulk prefetch of a global range into L2 (no shared-memory destination, no
-// completion): warms the 129 MB L2 ahead of the TMA loads that will read it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
-}
 
 // Programmatic dependent launch: let the next kernel start its prologue, and
 // wait for the previous kernel's writes before reading them.

@@ -124,6 +124,59 @@ def test_verify_rows_equal_decode_steps_bitwise(torch, tiny_cfg, tiny_prompt):
         assert int(am[j]) == int(amj[0])
 
 
+@pytest.mark.parametrize("shape", ["gqa-small", "qwen3-4b-1layer"])
+def test_grouped_rows_equal_decode_steps_bitwise(torch, shape):
+    """Batch invariance with grouped heads: a block of 16 tokens (64 query rows
+    per kv head, four row groups) and one of 8 (two row groups) against
+    one-token decode steps, bit for bit.  The attention unit splits its work
+    differently for 1, 2 and 4 row groups; every row must come out the same."""
+    if shape == "gqa-small":
+        cfg = small_gqa_cfg()
+    else:
+        cfg = synth.scaled(synth.qwen3_4b(max_ctx=512), n_layers=1)
+    w = synth.make_weights(cfg)
+    p = synth.prompt(cfg, 200, stream=5)
+    for n in (16, 8):
+        a = make_model(cfg, w)
+        b = make_model(cfg, w)
+        a.prefill(p[:130])
+        b.prefill(p[:130])
+        block = torch.tensor(p[130:130 + n], dtype=torch.int32, device="cuda")
+        am, _, lg, _ = a.verify(block, logits=True)
+        for j in range(n):
+            amj, _, lgj, _ = b.verify(block[j:j + 1].clone(), logits=True)
+            assert torch.equal(lg[j], lgj[0]), (shape, n, j)
+            assert int(am[j]) == int(amj[0])
+        a.close()
+        b.close()
+
+
+def test_launch_trace_records_every_launch(torch, tiny_cfg, tiny_prompt):
+    """spec_trace_*: a traced verify records, per launch, its kind and per-CTA
+    stamps in order (entry <= inputs ready <= exit)."""
+    import speculative_decoding_verify_pass_gb300 as sv
+    w = tiny_model_weights(tiny_cfg)
+    m = make_model(tiny_cfg, w)
+    m.prefill(tiny_prompt[:40])
+    sv.spec_trace_enable(m.h, True)
+    m.verify(torch.tensor(tiny_prompt[40:44], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    kinds = list(sv.spec_trace_kinds(m.h))
+    tr = sv.spec_trace_read(m.h)
+    sv.spec_trace_enable(m.h, False)
+    per_layer = [sv.EPI_QKV, 16, 17, sv.EPI_RESID, sv.EPI_SWIGLU, sv.EPI_RESID]
+    assert kinds == per_layer * tiny_cfg.n_layers + [sv.EPI_LMHEAD]
+    assert tr.shape[1] == len(kinds)
+    for l in range(len(kinds)):
+        s = tr[:, l, :]
+        live = s[s[:, 0] > 0]
+        assert len(live) > 0, l
+        assert np.all(live[:, 3] >= live[:, 0])
+        ready = live[live[:, 1] > 0]
+        assert np.all(ready[:, 1] >= ready[:, 0]) and np.all(ready[:, 3] >= ready[:, 1])
+    m.close()
+
+
 def test_rollback_equals_recompute_bitwise(torch, tiny_cfg, tiny_prompt):
     w = tiny_model_weights(tiny_cfg)
     a = make_model(tiny_cfg, w)
