@@ -149,6 +149,18 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------
+def reduce_over_ranks(dist, ms, tokens, device):
+    """Whole-job timing of N replicas: the slowest rank's time and the
+    tokens of all ranks."""
+    import torch
+    t = torch.tensor([ms, tokens], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    total = t.clone()
+    dist.all_reduce(total, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(total[1])
+
+
 def build_model(args, torch):
     import synth
     import speculative_decoding_verify_pass_gb300 as sv
@@ -256,12 +268,7 @@ def run_native(args):
     accepts = acc_log[args.warmup:total].cpu().numpy()
     tokens = float(np.sum(accepts + 1))
     if dist:
-        t = torch.tensor([ms, tokens], dtype=torch.float64, device="cuda")
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm_ = t.clone()
-        dist.all_reduce(sm_, op=dist.ReduceOp.SUM)
-        ms, tokens = float(mx[0]), float(sm_[1])
+        ms, tokens = reduce_over_ranks(dist, ms, tokens, "cuda")
     value = tokens / (ms / 1e3)
     ctx_now = m.kv_len(sv.SPEC_CACHE_TARGET)
 
@@ -440,12 +447,11 @@ def run_reference(args):
         return
     import oracle
     import synth
-    import speculative_decoding_verify_pass_gb300 as sv  # layer plan rule only
     oracle.build()
     synth.build()
     cfg = synth.PRESETS[args.config](max_ctx=args.ctx + 64)
     w = synth.make_weights(cfg)
-    plan = sv.layer_skip_plan(cfg.n_layers, args.skip)
+    plan = oracle.layer_skip_plan(cfg.n_layers, args.skip)
     orc, tc, dc = oracle_cycle_setup(cfg, w, plan, args.ctx)
     prompt = synth.prompt(cfg, args.ctx)
     y = int(prompt[-1])
