@@ -7,7 +7,8 @@
 // 2*n*N*K flops: the kernel is bound by HBM bandwidth, and its job is to keep
 // enough weight bytes in flight.
 //
-// Design (one CTA per SM, 8 consumer warps + 1 producer warp):
+// Design (one CTA per SM, 8 consumer warps + 1 producer warp + 1 operand
+// converter warp):
 //  * Weights are repacked once into 16 KB stages (128 rows x 64 k) laid out in
 //    mma.m16n8k16 A-fragment order, so a stage is one contiguous 1-D bulk copy
 //    (TMA engine, mbarrier completion) and each consumer lane reads its
@@ -15,7 +16,12 @@
 //  * The activation operand (n x 64 per stage) is kept by the producing kernel
 //    in B-fragment order and bulk-copied next to the weights: bf16 (<= 2 KB)
 //    for plain operands, fp32 x*gain (<= 4 KB) for RMS-normalised ones, which
-//    the consumers scale by rstd and round to bf16 while building fragments.
+//    the converter warp scales by rstd and rounds to bf16 in place, once per
+//    stage, before releasing the stage to the consumers.
+//  * A consumer warp takes the next stage together with the one after it when
+//    that one has already landed, and runs the two stages' MMA chains
+//    interleaved (the arithmetic of each stage is unchanged); the kernel is
+//    instantiated separately for one and two n8 token tiles.
 //  * A 10-deep ring of stages keeps 160 KB of weights in flight per SM.  The
 //    CTA takes over half of the SM's shared memory on purpose: a persistent
 //    grid with a static split must not have two of its CTAs on one SM.
@@ -41,8 +47,10 @@ namespace {
 
 using namespace gemm_core;
 
+constexpr int kGroup = 2;   // ring stages a consumer warp may take at once (4: slower, register cap)
+
 // --------------------------------------------------------------- kernel ---
-template <int EPI>
+template <int EPI, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw);
@@ -75,14 +83,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // ------- converter: fp32 operand stages -> bf16 fragments, once per stage -------
         if (!p.x_f32) return;
         named_bar_sync(2, kConsumers + 32);   // the consumers' rstd is in shared memory
-        const bool two = p.n > 8;
         StageIter it;
         it.init(p, n_items);
         bool aborted = false;
         for (int q = 0; it.valid; ++q) {
             const int s = q % kStages;
             if (!aborted && !mbar_wait(&sm.full[s], (q / kStages) & 1, err, 4)) aborted = true;
-            convert_stage(sm.x[s], two, sm.rstd_op, lane);
+            convert_stage<TWO>(sm.x[s], sm.rstd_op, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.ready[s]);
             it.advance();
@@ -151,7 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
     StageIter it;
     it.init(p, n_items);
-    const bool two = p.n > 8;
     // fp32 operands reach the consumers already converted (ready barrier)
     uint64_t* gate = p.x_f32 ? sm.ready : sm.full;
     int q = 0;
@@ -160,12 +166,27 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     while (it.valid) {
         const int tile = it.tile, item = it.item, b0 = it.b, b1 = it.b1;
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int b = b0; b < b1; ++b, ++q) {
-            const int s = q % kStages;
-            if (!aborted && !mbar_wait(&gate[s], (q / kStages) & 1, err, 1)) aborted = true;
-            mma_stage(sm, s, warp, lane, two, false, 1.f, 1.f, acc0, acc1);
+        for (int b = b0; b < b1;) {
+            // the next stage, and as many of the following ones (up to
+            // kGroup in all) as have already landed
+            int st[4];
+            st[0] = q % kStages;
+            if (!aborted && !mbar_wait(&gate[st[0]], (q / kStages) & 1, err, 1)) aborted = true;
+            int m = 1;
+            while (m < kGroup && b + m < b1) {
+                const int qq = q + m;
+                if (!aborted && !mbar_test(&gate[qq % kStages], (qq / kStages) & 1)) break;
+                st[m++] = qq % kStages;
+            }
+            if (kGroup >= 4 && m == 4) mma_stages<4, TWO>(sm, st, warp, lane, acc0, acc1);
+            else if (kGroup >= 3 && m == 3) mma_stages<3, TWO>(sm, st, warp, lane, acc0, acc1);
+            else if (kGroup >= 2 && m == 2) mma_stages<2, TWO>(sm, st, warp, lane, acc0, acc1);
+            else mma_stages<1, TWO>(sm, st, warp, lane, acc0, acc1);
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            if (lane == 0)
+                for (int u = 0; u < m; ++u) mbar_arrive(&sm.empty[st[u]]);
+            b += m;
+            q += m;
         }
         // the segment of the CTA's range that lies in this tile is done
         it.valid = it.next_seg();
@@ -190,12 +211,17 @@ cudaError_t launch_one(const GemmParams& p, cudaStream_t s, bool pdl) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI>, p);
+    if (p.n > 8) return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, true>, p);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<EPI, false>, p);
 }
 
 template <int EPI>
 cudaError_t configure_one() {
-    return cudaFuncSetAttribute(gemm_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(GemmSmem));
+    const cudaError_t e = cudaFuncSetAttribute(gemm_kernel<EPI, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)sizeof(GemmSmem));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(gemm_kernel<EPI, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sizeof(GemmSmem));
 }
 
 }  // namespace

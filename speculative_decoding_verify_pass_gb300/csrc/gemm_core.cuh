@@ -528,15 +528,56 @@ __device__ __forceinline__ void mma_stage(const GemmSmem& sm, int s, int warp, i
     }
 }
 
+// P ring stages (bf16 operands) at once: the stages' MMA chains are
+// independent, so issuing them interleaved hides the tensor-core latency that
+// a single four-deep chain exposes.  TWO (n > 8: a second n8 token tile) is a
+// compile-time choice: a run-time branch around the MMAs inside this loop
+// costs about three times the loop's own time.  The arithmetic is exactly mma_stage's,
+// stage by stage: every stage's four k16 products start from zero, and the
+// stage sums are added to the running accumulator in stage order.
+template <int P, bool TWO>
+__device__ __forceinline__ void mma_stages(const GemmSmem& sm, const int (&st)[4], int warp, int lane,
+                                           float (&run0)[4], float (&run1)[4]) {
+    float acc0[P][4], acc1[P][4];
+#pragma unroll
+    for (int u = 0; u < P; ++u)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc0[u][i] = acc1[u][i] = 0.f;
+#pragma unroll
+    for (int k16 = 0; k16 < 4; ++k16) {
+#pragma unroll
+        for (int u = 0; u < P; ++u) {
+            const uint8_t* ws = sm.w[st[u]] + warp * 2048 + lane * 16;
+            const uint8_t* xs = sm.x[st[u]] + lane * 8;
+            const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
+            const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
+            const uint2 bv = *reinterpret_cast<const uint2*>(xs + k16 * 256);
+            mma_bf16_16816(acc0[u], a, bv.x, bv.y);
+            if constexpr (TWO) {
+                const uint2 bw = *reinterpret_cast<const uint2*>(xs + 1024 + k16 * 256);
+                mma_bf16_16816(acc1[u], a, bw.x, bw.y);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < P; ++u)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            run0[i] += acc0[u][i];
+            if constexpr (TWO) run1[i] += acc1[u][i];
+        }
+}
+
 // Converts one ring stage's fp32 operand (x*gain, fp32 fragment order) in
 // place into bf16 B fragments of x*gain*rstd (the layout bf16 operands use),
 // by one warp: each lane reads its entries for every (n8, k16) first, then
 // writes, so the half-size output cannot overwrite unread input.  The
 // rounding is the one the consumers would otherwise do: fp32 product, then
 // bf16 round-to-nearest-even.
-__device__ __forceinline__ void convert_stage(uint8_t* xs, bool two, const float* rstd_op, int lane) {
+template <bool TWO>
+__device__ __forceinline__ void convert_stage(uint8_t* xs, const float* rstd_op, int lane) {
     float4 v[8];
-    const int entries = two ? 8 : 4;   // (n8, k16) pairs
+    constexpr int entries = TWO ? 8 : 4;   // (n8, k16) pairs
 #pragma unroll
     for (int t = 0; t < 8; ++t)
         if (t < entries) v[t] = *reinterpret_cast<const float4*>(xs + (t * 32 + lane) * 16);
