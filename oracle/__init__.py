@@ -86,7 +86,7 @@ def _load(acc64: bool = False):
         lib.orc_cache_set_len.restype = i32
         lib.orc_cache_read.argtypes = [vp, i32, i32, i32, vp]
         lib.orc_cache_read.restype = i32
-        lib.orc_forward.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp]
+        lib.orc_forward.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
         lib.orc_forward.restype = i32
         lib.orc_argmax.argtypes = [vp, i32]
         lib.orc_argmax.restype = i32
@@ -257,11 +257,12 @@ class Oracle:
         return Cache(self, self.cfg.n_layers if n_slots is None else n_slots)
 
     def forward(self, cache: Cache, plan, tokens, pos0: int, logits_from: int | None = 0,
-                want_routing: bool = False, forced_ids=None, probs=None):
+                want_routing: bool = False, forced_ids=None, probs=None, hidden=None):
         """Run ``tokens`` at positions pos0.. through ``plan``; returns
         (logits[rows][V] or None, ids or None, gates or None).  ``probs``, a
         float32 array [len(plan)][n][n_experts], receives the router
-        probabilities of the MoE layers."""
+        probabilities of the MoE layers; ``hidden``, a float32 array
+        [len(plan)][n][d_model], the residual stream after each layer."""
         plan_a = np.ascontiguousarray(plan, dtype=np.int32)
         tok = np.ascontiguousarray(tokens, dtype=np.int32)
         n = len(tok)
@@ -280,13 +281,17 @@ class Oracle:
         if probs is not None:
             assert probs.dtype == np.float32 and probs.flags.c_contiguous
             assert probs.shape == (len(plan_a), n, c.n_experts)
+        if hidden is not None:
+            assert hidden.dtype == np.float32 and hidden.flags.c_contiguous
+            assert hidden.shape == (len(plan_a), n, c.d_model)
         rc = self._lib.orc_forward(self.h, cache.h, _ptr(plan_a), len(plan_a), _ptr(tok), n, int(pos0),
                                    _ptr(logits) if logits is not None else None,
                                    int(logits_from) if logits is not None else 0,
                                    _ptr(ids) if ids is not None else None,
                                    _ptr(gates) if gates is not None else None,
                                    _ptr(forced) if forced is not None else None,
-                                   _ptr(probs) if probs is not None else None)
+                                   _ptr(probs) if probs is not None else None,
+                                   _ptr(hidden) if hidden is not None else None)
         if rc != 0:
             raise ValueError("oracle forward rejected its arguments")
         return logits, ids, gates

@@ -354,11 +354,15 @@ static void ffn_swiglu(const uint16_t* wg, const uint16_t* wu, const uint16_t* w
  * NULL) receives every router probability of every MoE layer, so that a
  * caller can check a forced choice against the top-k it replaced.
  *
+ * hidden_out ([plan_len][n][d_model], may be NULL) receives the residual
+ * stream after each executed layer: the target hidden states from which the
+ * mlx-dflash README ("Architecture") takes the draft's context features.
+ *
  * Returns 0, or 1 on a bad argument (pos0 beyond the cache length, overflow).
  */
 int orc_forward(const orc_model* m, orc_cache* cache, const int* plan, int plan_len, const int* tokens,
                 int n, int pos0, float* logits, int logits_from, int* ids_out, float* gates_out,
-                const int* forced_ids, float* probs_out) {
+                const int* forced_ids, float* probs_out, float* hidden_out) {
     const orc_cfg* c = &m->c;
     const int d = c->d_model, hd = c->head_dim, Hq = c->n_heads, Hkv = c->n_kv_heads;
     const int qw = Hq * hd, kw = Hkv * hd, group = Hq / Hkv;
@@ -444,6 +448,7 @@ int orc_forward(const orc_model* m, orc_cache* cache, const int* plan, int plan_
             ffn_swiglu(m->gate[l], m->up[l], m->down[l], d, c->ffn_dim, h, n, y);
         }
         for (size_t e = 0; e < (size_t)n * d; ++e) x[e] += y[e];
+        if (hidden_out) memcpy(hidden_out + (size_t)s * n * d, x, sizeof(float) * (size_t)n * d);
     }
     cache->len = pos0 + n;
 

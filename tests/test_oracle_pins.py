@@ -245,10 +245,16 @@ def test_router_topk_against_sort():
 # Whole forward: first token at position 0 against a float64 library path
 # ----------------------------------------------------------------------------
 def _ref_first_token_logits(cfg, w, token):
+    return _ref_first_token(cfg, w, token)[0]
+
+
+def _ref_first_token(cfg, w, token):
     """At position 0 the rotation is the identity and each query sees one key,
     so attention returns v exactly; the rest is library float64 matmuls with
-    the same bf16 rounding points."""
+    the same bf16 rounding points.  Returns (logits, residual after each
+    layer)."""
     d, eps = cfg.d_model, cfg.norm_eps
+    xs = []
     x = widen(w.embed[token])
 
     def norm(v, g):
@@ -277,7 +283,8 @@ def _ref_first_token_logits(cfg, w, token):
             x = x + y
         else:
             x = x + ffn(h, L["w_gate"], L["w_up"], L["w_down"])
-    return widen(w.lm_head_or_embed()) @ norm(x, w.final_norm)
+        xs.append(x)
+    return widen(w.lm_head_or_embed()) @ norm(x, w.final_norm), xs
 
 
 @pytest.mark.parametrize("make", ["tiny", "gqa", "moe"])
@@ -296,6 +303,48 @@ def test_first_token_forward_matches_library_path(make):
         scale = np.max(np.abs(ref))
         assert np.max(err) < 2e-2 * scale, (make, token, np.max(err), scale)
         assert np.mean(err) < 2e-3 * scale
+
+
+@pytest.mark.parametrize("make", ["tiny", "gqa", "moe"])
+def test_hidden_states_match_library_path(make):
+    """The residual stream after every layer (the target hidden states the
+    mlx-dflash README's draft conditions on), against the float64 library
+    path at position 0."""
+    cfg = {"tiny": synth.tiny(), "gqa": small_gqa_cfg(), "moe": small_moe_cfg()}[make]
+    w = synth.make_weights(cfg)
+    orc = oracle.Oracle(cfg, w)
+    for token in (3, cfg.vocab - 2):
+        hid = np.zeros((cfg.n_layers, 1, cfg.d_model), np.float32)
+        orc.forward(orc.new_cache(), orc.full_plan, [token], 0, hidden=hid)
+        _, xs = _ref_first_token(cfg, w, token)
+        for l in range(cfg.n_layers):
+            err = np.abs(hid[l, 0] - xs[l])
+            scale = np.max(np.abs(xs[l]))
+            assert np.max(err) < 2e-2 * scale and np.mean(err) < 2e-3 * scale, (make, token, l)
+
+
+def test_hidden_state_taps_residual_identity_and_logits(tiny_prompt):
+    """A layer whose O and down projections are zero leaves the residual
+    stream unchanged, bit for bit; and the final norm and LM head applied to
+    the last layer's hidden state give the oracle's logits."""
+    import copy
+    cfg = small_gqa_cfg()
+    w = copy.deepcopy(synth.make_weights(cfg))
+    L1 = w.layers[1]
+    L1["wo"] = np.zeros_like(L1["wo"])
+    L1["w_down"] = np.zeros_like(L1["w_down"])
+    orc = oracle.Oracle(cfg, w)
+    toks = [int(t) % cfg.vocab for t in tiny_prompt[:9]]
+    hid = np.zeros((cfg.n_layers, len(toks), cfg.d_model), np.float32)
+    lg, _, _ = orc.forward(orc.new_cache(), orc.full_plan, toks, 0, hidden=hid)
+    assert np.array_equal(hid[1], hid[0])
+    assert not np.array_equal(hid[2], hid[1])
+    x = hid[-1].astype(np.float64)
+    g = widen(w.final_norm)
+    h = bf16_np(x / np.sqrt(np.mean(x * x, axis=1, keepdims=True) + cfg.norm_eps) * g)
+    ref = h @ widen(w.lm_head_or_embed()).T
+    assert np.max(np.abs(lg - ref)) < 1e-3 * np.max(np.abs(ref))
+    assert [int(np.argmax(r)) for r in lg] == [int(np.argmax(r)) for r in ref]
 
 
 # ----------------------------------------------------------------------------
