@@ -627,6 +627,9 @@ def suite_geometric(args):
     m.close()
 
 
+DFLASH_TAP_LAYERS = [1, 9, 17, 25, 33]
+
+
 def suite_dflash(args):
     """Qwen3-8B verify of a 16-token block (the DFlash block size) at context
     1024/2048/4096, accept lengths truncated-geometric with mean 6 and 9, then
@@ -644,6 +647,14 @@ def suite_dflash(args):
         ac = torch.zeros(1, dtype=torch.int32, device="cuda")
         us_v = _time_calls(torch, lambda: (sv.spec_verify_step(m.h, blk, am, ac), m.kv_set_len(0, ctx)), 10)
         us_set = _time_calls(torch, lambda: m.kv_set_len(0, ctx), 20)
+        # the same verify writing the hidden states the DFlash draft conditions on
+        # (the README's "Architecture": layers 1, 9, 17, 25, 33)
+        m.set_taps(DFLASH_TAP_LAYERS)
+        us_taps = _time_calls(torch, lambda: (sv.spec_verify_step(m.h, blk, am, ac), m.kv_set_len(0, ctx)), 10)
+        m.set_taps([])
+        _emit({"suite": "dflash_taps", "config": "qwen3-8b", "ctx": ctx, "n": 16, "layers": DFLASH_TAP_LAYERS,
+               "verify_us": round(us_v - us_set, 1), "verify_us_with_taps": round(us_taps - us_set, 1),
+               "tap_bytes": len(DFLASH_TAP_LAYERS) * 16 * cfg.d_model * 4})
         for mean in (6.0, 9.0):
             alpha = stepmodel.alpha_for_mean_accept(mean, 15)
             ks = synth.geometric_accept_lengths(64, alpha, 15, stream=int(mean))

@@ -186,6 +186,22 @@ spec_status spec_kv_rollback(spec_handle h, int32_t which, int32_t new_len);
  * bitwise identical outputs. */
 spec_status spec_moe_mode(spec_handle h, int32_t mode);
 
+/* Hidden-state taps (mlx-dflash README, "Architecture": the draft's context
+ * features are taken from the target's hidden states at chosen layers).
+ * After this call every target verify pass also writes, for each of its n
+ * rows, the residual stream after layer layers[t] (fp32, the value the next
+ * layer's norm reads) to d_out[(t * 16 + row) * d_model ...].  Rows n..15
+ * are left untouched; prefill and draft passes write nothing.
+ *   layers  host array of `count` distinct layer indices in [0, n_layers);
+ *   count   0..n_layers; 0 switches the taps off (layers, d_out may be NULL);
+ *   d_out   device buffer of count * 16 * d_model floats, 16-byte aligned,
+ *           CALLER-owned; it must stay valid while taps are on.
+ * Synchronises the stream and drops captured launch sequences.  Errors:
+ * SPEC_ERR_INVALID_ARG (range, duplicates, alignment, NULL), state unchanged.
+ * Taps run on the separate-launch path (the opt-in persistent pass kernel is
+ * not used while they are on). */
+spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, float* d_out);
+
 /* Thread-local description of the last error. */
 const char* spec_last_error(void);
 

@@ -26,7 +26,8 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_draft_step", "spec_verify_step", "spec_kv_rollback", "spec_moe_mode", "spec_last_error",
             "spec_check_error", "spec_kv_len", "spec_kv_load", "spec_kv_export", "spec_kv_set_len",
             "spec_moe_force_routing", "spec_last_launch_count", "spec_profile_enable", "spec_profile_read",
-            "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds"]
+            "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds",
+            "spec_set_taps"]
 
 
 class SpecError(RuntimeError):
@@ -80,6 +81,7 @@ def library():
         "spec_verify_step": [vp, vp, i32, vp, vp, vp, vp, vp],
         "spec_kv_rollback": [vp, i32, i32],
         "spec_moe_mode": [vp, i32],
+        "spec_set_taps": [vp, vp, i32, vp],
         "spec_check_error": [vp],
         "spec_kv_len": [vp, i32, ctypes.POINTER(i32)],
         "spec_kv_load": [vp, i32, i32, vp, vp, i32],
@@ -141,6 +143,14 @@ def spec_kv_rollback(h, which: int, new_len: int):
 
 def spec_moe_mode(h, mode: int):
     _check(library().spec_moe_mode(h, int(mode)))
+
+
+def spec_set_taps(h, layers, d_out=None):
+    """Hidden-state taps: the residual stream after each of ``layers`` is
+    written by every target verify pass to ``d_out`` [len(layers)][16][d_model]
+    (fp32, device).  An empty list switches them off."""
+    arr = (ctypes.c_int32 * max(len(layers), 1))(*[int(l) for l in layers])
+    _check(library().spec_set_taps(h, arr if layers else None, len(layers), _ptr(d_out)))
 
 
 def spec_check_error(h):
@@ -329,6 +339,16 @@ class Model:
 
     def moe_mode(self, mode):
         spec_moe_mode(self.h, mode)
+
+    def set_taps(self, layers):
+        """Tap the residual stream after ``layers`` in every verify pass;
+        returns the fp32 device buffer [len(layers)][16][d_model] the passes
+        write (None when ``layers`` is empty)."""
+        self._taps = None
+        if layers:
+            self._taps = self._torch.zeros((len(layers), 16, self.cfg.d_model), dtype=self._torch.float32, device="cuda")
+        spec_set_taps(self.h, list(layers), self._taps)
+        return self._taps
 
     def check_error(self):
         spec_check_error(self.h)

@@ -89,6 +89,9 @@ struct spec_model {
     float* route_gates = nullptr;
     int* forced = nullptr;
     bool forced_on = false;
+    std::vector<int> tap_of_layer;      // hidden-state taps: slot of each layer in tap_out, or -1
+    float* tap_out = nullptr;           // caller's [count][16][d_model] fp32 buffer
+    int tap_count = 0;
     float* y_slot = nullptr;
     float* ys = nullptr;
     DevState* st = nullptr;
@@ -385,7 +388,7 @@ void clear_graphs(spec_model* h) {
 spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
                      int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair, int32_t* d_token,
                      const int32_t* d_block) {
-    if (h->use_pass && h->c.n_experts == 0)
+    if (h->use_pass && h->c.n_experts == 0 && h->tap_count == 0)
         return run_pass_kernel(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_pair, d_token, d_block);
     if (h->trace) {  // a traced pass runs its launches directly, each with its own stamp slots
         h->trace_mode = 2;
@@ -400,7 +403,8 @@ spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, P
     const std::vector<uintptr_t> key = {(uintptr_t)which, (uintptr_t)n, (uintptr_t)mode, (uintptr_t)d_tokens,
                                         (uintptr_t)d_argmax, (uintptr_t)d_accept, (uintptr_t)d_logits,
                                         (uintptr_t)d_ids, (uintptr_t)d_pair, (uintptr_t)d_token, (uintptr_t)d_block,
-                                        (uintptr_t)h->moe_mode, (uintptr_t)h->forced_on};
+                                        (uintptr_t)h->moe_mode, (uintptr_t)h->forced_on, (uintptr_t)h->tap_out,
+                                        (uintptr_t)h->tap_count};
     auto f = h->graphs.find(key);
     if (f == h->graphs.end()) {
         if (h->graphs.size() >= 256) clear_graphs(h);
@@ -460,6 +464,10 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         const int l = plan[si];
         LayerW& W = h->L[l];
         const uint16_t* g_after = (si + 1 < plan.size()) ? h->L[plan[si + 1]].attn_norm : h->final_norm;
+        // hidden-state tap: the residual stream after this layer, target verify passes only
+        float* tap = (which == 0 && mode == PASS_VERIFY && h->tap_count > 0 && h->tap_of_layer[l] >= 0)
+                         ? h->tap_out + (size_t)h->tap_of_layer[l] * kMaxBlock * d
+                         : nullptr;
         uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
         uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
 
@@ -511,6 +519,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             set_mat(h, p, W.down, h->xf_down, EPI_RESID, G);
             p.g_next = g_after;
             p.xf_out = h->xf_norm;
+            p.tap = tap;
             if ((s = gemm(h, p)) != SPEC_OK) return s;
         } else {
             const int K = c.top_k;
@@ -569,6 +578,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             cb.g_next = g_after;
             cb.xf_out = h->xf_norm;
             cb.ss_out = h->ss;
+            cb.tap = tap;
             CU(launch_moe_combine(cb, h->stream, pdl));
             ++h->launches;
         }
@@ -1109,6 +1119,27 @@ spec_status spec_moe_mode(spec_handle h, int32_t mode) {
     if (mode != SPEC_MOE_PER_SLOT && mode != SPEC_MOE_DEDUP) return fail(SPEC_ERR_INVALID_ARG, "bad MoE mode");
     if (h->c.n_experts == 0) return fail(SPEC_ERR_STATE, "dense model");
     h->moe_mode = mode;
+    return SPEC_OK;
+}
+
+spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, float* d_out) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (count < 0 || count > h->c.n_layers) return fail(SPEC_ERR_INVALID_ARG, "tap count %d out of range", count);
+    if (count > 0 && (!layers || !d_out)) return fail(SPEC_ERR_INVALID_ARG, "null tap layers or output");
+    if (count > 0 && (reinterpret_cast<uintptr_t>(d_out) & 15))
+        return fail(SPEC_ERR_INVALID_ARG, "tap output not 16-byte aligned");
+    std::vector<int> of(h->c.n_layers, -1);
+    for (int t = 0; t < count; ++t) {
+        const int l = layers[t];
+        if (l < 0 || l >= h->c.n_layers) return fail(SPEC_ERR_INVALID_ARG, "tap layer %d out of range", l);
+        if (of[l] >= 0) return fail(SPEC_ERR_INVALID_ARG, "tap layer %d listed twice", l);
+        of[l] = t;
+    }
+    CU(cudaStreamSynchronize(h->stream));
+    clear_graphs(h);
+    h->tap_of_layer = of;
+    h->tap_out = count > 0 ? d_out : nullptr;
+    h->tap_count = count;
     return SPEC_OK;
 }
 

@@ -221,6 +221,11 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             }
             *reinterpret_cast<float4*>(xr) = make_float4(v[0], v[1], v[2], v[3]);
             *reinterpret_cast<float4*>(xr + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            if (p.tap) {
+                float* tr = p.tap + (size_t)j * p.d + R0;
+                *reinterpret_cast<float4*>(tr) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(tr + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            }
         }
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);

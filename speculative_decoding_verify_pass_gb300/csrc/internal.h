@@ -78,6 +78,7 @@ struct GemmParams {
     const uint16_t* g_next;    // gain of the norm that consumes x next
     uint8_t* xf_out;           // next GEMM's operand
     float* ss_out;             // [16][d/128]
+    float* tap;                // optional: the new residual rows, fp32 [16][d] (hidden-state tap)
     // EPI_LMHEAD
     float* logits;             // optional [n][vocab]
     float* amax_val;           // [16][T]
@@ -139,6 +140,7 @@ struct CombineParams {           // MoE: x += sum_s gate*y_slot + y_shared
     const uint16_t* g_next;
     uint8_t* xf_out;
     float* ss_out;
+    float* tap;                // optional: the new residual rows, fp32 [16][d] (hidden-state tap)
 };
 cudaError_t launch_moe_combine(const CombineParams& p, cudaStream_t s, bool pdl);
 

@@ -110,6 +110,11 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant_
             if (p.y_shared) t += p.y_shared[(size_t)j * p.d + R0 + e];
             v[e] = xv[e] + t;
         }
+        if (p.tap) {
+            float* tr = p.tap + (size_t)j * p.d + R0;
+            *reinterpret_cast<float4*>(tr) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(tr + 4) = make_float4(v[4], v[5], v[6], v[7]);
+        }
         ssum = store_residual8(xr, v, j, R0, p.g_next, p.xf_out);
     }
 #pragma unroll
