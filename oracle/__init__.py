@@ -88,6 +88,8 @@ def _load(acc64: bool = False):
         lib.orc_cache_read.restype = i32
         lib.orc_forward.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
         lib.orc_forward.restype = i32
+        lib.orc_context_append.argtypes = [vp, vp, vp, i32, vp, i32, vp]
+        lib.orc_context_append.restype = i32
         lib.orc_argmax.argtypes = [vp, i32]
         lib.orc_argmax.restype = i32
         lib.orc_bf16_round.argtypes = [ctypes.c_float]
@@ -295,6 +297,23 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle forward rejected its arguments")
         return logits, ids, gates
+
+
+    def context_append(self, cache: Cache, fc_bits: np.ndarray, taps: np.ndarray, rows: int) -> np.ndarray:
+        """The block draft's conditioning (mlx-dflash README, "Architecture"):
+        features = fc . bf16(concat of the taps of rows 0..rows-1), then every
+        layer appends the keys and values of those positions computed from the
+        features.  fc_bits: bf16 bits [d_model][n_in * d_model]; taps: float32
+        [n_in][16][d_model].  Returns the features [rows][d_model]."""
+        c = self.cfg
+        fc = np.ascontiguousarray(fc_bits, dtype=np.uint16)
+        tp = np.ascontiguousarray(taps, dtype=np.float32)
+        n_in = tp.shape[0]
+        assert tp.shape == (n_in, 16, c.d_model) and fc.shape == (c.d_model, n_in * c.d_model)
+        feat = np.empty((rows, c.d_model), dtype=np.float32)
+        if self._lib.orc_context_append(self.h, cache.h, _ptr(fc), n_in, _ptr(tp), int(rows), _ptr(feat)) != 0:
+            raise ValueError("oracle context append rejected its arguments")
+        return feat
 
 
 # ----------------------------------------------------------------------------

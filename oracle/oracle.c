@@ -465,6 +465,63 @@ int orc_forward(const orc_model* m, orc_cache* cache, const int* plan, int plan_
     return 0;
 }
 
+/* ------------------------------------------------ DFlash context append --- */
+/*
+ * The conditioning path of the block draft in the mlx-dflash README
+ * ("Architecture"): the target hidden states tapped at n_in layers are
+ * projected by fc into one context feature per position, and the draft
+ * attends over those context positions.  Reading: each layer of this model
+ * computes the keys and values of a context position from its feature the
+ * way it computes them from a token's residual stream (that layer's input
+ * norm, its k and v projections, RoPE on k at the position), and appends them
+ * to its cache; nothing else of the layer runs.
+ *
+ * taps: fp32 [n_in][16][d_model], rows r < m used (the tap buffer layout).
+ * fc:   bf16 [d_model][n_in * d_model], input index t * d_model + i.
+ * The concatenated taps are rounded to bf16 (a GEMM operand); the feature is
+ * the fp32 product.  Positions len .. len + m - 1 of every slot (slot s =
+ * layer s; the cache must cover every layer) are written, then len += m.
+ * feat_out (may be NULL) receives the features, fp32 [m][d_model].
+ * Returns 0, or 1 on a bad argument.
+ */
+int orc_context_append(const orc_model* m, orc_cache* cache, const uint16_t* fc, int n_in, const float* taps,
+                       int rows, float* feat_out) {
+    const orc_cfg* c = &m->c;
+    const int d = c->d_model, hd = c->head_dim, Hkv = c->n_kv_heads, kw = Hkv * hd;
+    if (n_in < 1 || rows < 1 || rows > 16 || cache->n_slots != c->n_layers) return 1;
+    if (cache->len + rows > cache->max_ctx) return 1;
+    const int K = n_in * d;
+    float* xin = (float*)malloc(sizeof(float) * (size_t)rows * K);
+    float* feat = (float*)malloc(sizeof(float) * (size_t)rows * d);
+    float* h = (float*)malloc(sizeof(float) * (size_t)rows * d);
+    float* kk = (float*)malloc(sizeof(float) * (size_t)rows * kw);
+    float* vv = (float*)malloc(sizeof(float) * (size_t)rows * kw);
+    for (int r = 0; r < rows; ++r)
+        for (int t = 0; t < n_in; ++t)
+            for (int i = 0; i < d; ++i)
+                xin[(size_t)r * K + (size_t)t * d + i] = bf_round(taps[((size_t)t * 16 + r) * d + i]);
+    gemm_rows(fc, d, K, xin, rows, feat);
+    if (feat_out) memcpy(feat_out, feat, sizeof(float) * (size_t)rows * d);
+    for (int l = 0; l < c->n_layers; ++l) {
+        for (int r = 0; r < rows; ++r) rmsnorm_bf16(feat + (size_t)r * d, m->attn_norm[l], d, c->norm_eps, h + (size_t)r * d);
+        gemm_rows(m->wk[l], kw, d, h, rows, kk);
+        gemm_rows(m->wv[l], kw, d, h, rows, vv);
+        float* ck = cache->k + (size_t)l * cache->max_ctx * kw;
+        float* cv = cache->v + (size_t)l * cache->max_ctx * kw;
+        for (int r = 0; r < rows; ++r) {
+            const int pos = cache->len + r;
+            for (int hh = 0; hh < Hkv; ++hh) rope_apply(m, kk + (size_t)r * kw + hh * hd, pos);
+            for (int e = 0; e < kw; ++e) {
+                ck[(size_t)pos * kw + e] = bf_round(kk[(size_t)r * kw + e]);
+                cv[(size_t)pos * kw + e] = bf_round(vv[(size_t)r * kw + e]);
+            }
+        }
+    }
+    cache->len += rows;
+    free(xin); free(feat); free(h); free(kk); free(vv);
+    return 0;
+}
+
 /* Index of the largest value; the lowest index wins ties. */
 int orc_argmax(const float* v, int count) {
     int best = 0;

@@ -506,3 +506,61 @@ def test_moe_per_token_routing_recorded():
             top = sorted(range(cfg.n_experts), key=lambda e: (-pr[e], e))[:cfg.top_k]
             assert list(ids[l, t]) == top
             assert np.array_equal(gates2[l, t], probs[l, t][ids[l, t]])
+
+
+# ----------------------------------------------------------------------------
+# Block-draft conditioning (mlx-dflash README, "Architecture")
+# ----------------------------------------------------------------------------
+def _identity_bits(d):
+    eye = np.zeros((d, d), np.uint16)
+    eye[np.arange(d), np.arange(d)] = 0x3F80          # bf16 1.0
+    return eye
+
+
+def test_context_append_of_embeddings_reproduces_layer0_kv():
+    """With fc the identity and the taps holding token embeddings (exact in
+    bf16), the features are the embeddings themselves and layer 0's appended
+    keys and values are, bit for bit, those a forward of the same tokens
+    writes: the appended path is layer 0's k/v path."""
+    cfg = small_gqa_cfg()
+    w = synth.make_weights(cfg)
+    orc = oracle.Oracle(cfg, w)
+    toks = synth.prompt(cfg, 11, stream=4)
+    taps = np.zeros((1, 16, cfg.d_model), np.float32)
+    taps[0, :11] = widen(w.embed[toks])
+    ca = orc.new_cache()
+    feat = orc.context_append(ca, _identity_bits(cfg.d_model), taps, 11)
+    assert np.array_equal(feat, taps[0, :11]) and ca.len == 11
+    cb = orc.new_cache()
+    orc.forward(cb, orc.full_plan, toks, 0, logits_from=None)
+    for which in (0, 1):
+        assert np.array_equal(ca.read(0, which, 11), cb.read(0, which, 11))
+    assert not np.array_equal(ca.read(1, 0, 11), cb.read(1, 0, 11))   # layer 1 saw other inputs
+
+
+def test_context_append_fc_and_position_continuity():
+    """fc against a float64 library matmul of the bf16-rounded concatenation;
+    appending 5 rows then 6 equals appending the 11 at once, bit for bit (each
+    row is independent and positions continue from the cache length)."""
+    cfg = small_gqa_cfg()
+    w = synth.make_weights(cfg)
+    orc = oracle.Oracle(cfg, w)
+    d, n_in = cfg.d_model, 3
+    fc = synth.normal_bf16((d, n_in * d), 21, 1)
+    rng = np.random.default_rng(7)
+    taps = rng.standard_normal((n_in, 16, d)).astype(np.float32)
+    c1 = orc.new_cache()
+    feat = orc.context_append(c1, fc, taps, 11)
+    concat = np.concatenate([bf16_np(taps[t, :11].astype(np.float64)) for t in range(n_in)], axis=1)
+    ref = concat @ widen(fc).T
+    assert np.max(np.abs(feat - ref)) < 1e-5 * np.max(np.abs(ref))
+    c2 = orc.new_cache()
+    first = taps.copy()
+    orc.context_append(c2, fc, first, 5)
+    second = np.zeros_like(taps)
+    second[:, :6] = taps[:, 5:11]
+    orc.context_append(c2, fc, second, 6)
+    assert c2.len == 11
+    for l in range(cfg.n_layers):
+        for which in (0, 1):
+            assert np.array_equal(c1.read(l, which, 11), c2.read(l, which, 11))
