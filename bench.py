@@ -676,6 +676,60 @@ def suite_dflash(args):
         torch.cuda.empty_cache()
 
 
+def suite_dflash_block(args):
+    """A DFlash-shaped cycle on Qwen3-8B shapes at context 2048 (random
+    weights, so timing only): the target's verify of a 16-token block with
+    hidden-state taps at layers 1, 9, 17, 25, 33; the draft's context append
+    of the m new positions (fc 5*4096 -> 4096, then each draft layer's context
+    keys/values); the 5-layer block draft over [last token, mask x 15]; both
+    rollbacks.  m = accept + 1 for the mean accept lengths 6 and 9."""
+    import numpy as np
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    ctx = 2048
+    cfg_t = synth.qwen3_8b(max_ctx=ctx + 64)
+    cfg_d = synth.scaled(cfg_t, n_layers=5)
+    mt, _ = _model_at_context(cfg_t, ctx)
+    md, _ = _model_at_context(cfg_d, ctx)
+    taps = mt.set_taps(DFLASH_TAP_LAYERS)
+    fc = synth.normal_bf16((cfg_t.d_model, len(DFLASH_TAP_LAYERS) * cfg_t.d_model), 41, 1)
+    md.set_context_fc(fc)
+    blk_t = torch.tensor(synth.prompt(cfg_t, 16).tolist(), dtype=torch.int32, device="cuda")
+    blk_d = torch.tensor([int(blk_t[0])] + [cfg_d.vocab - 1] * 15, dtype=torch.int32, device="cuda")
+    am = torch.zeros(16, dtype=torch.int32, device="cuda")
+    ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+    am2 = torch.zeros(16, dtype=torch.int32, device="cuda")
+    ac2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    us_set = _time_calls(torch, lambda: mt.kv_set_len(0, ctx), 20)
+    us_verify = _time_calls(torch, lambda: (sv.spec_verify_step(mt.h, blk_t, am, ac), mt.kv_set_len(0, ctx)), 10) - us_set
+    us_block = _time_calls(torch, lambda: (sv.spec_verify_step(md.h, blk_d, am2, ac2), md.kv_set_len(0, ctx)), 10) - us_set
+    for mean in (6.0, 9.0):
+        rows = int(round(mean)) + 1
+        us_app = _time_calls(torch, lambda: (sv.spec_context_append(md.h, taps, rows), md.kv_set_len(0, ctx)), 10) - us_set
+
+        def cycle():
+            sv.spec_verify_step(mt.h, blk_t, am, ac)
+            mt.kv_set_len(0, ctx)
+            sv.spec_context_append(md.h, taps, rows)
+            sv.spec_verify_step(md.h, blk_d, am2, ac2)
+            md.kv_set_len(0, ctx)
+        us_cycle = _time_calls(torch, cycle, 10) - 2 * us_set
+        alpha = stepmodel.alpha_for_mean_accept(mean, 15)
+        ks = synth.geometric_accept_lengths(64, alpha, 15, stream=int(mean))
+        toks = float(np.mean(ks + 1))
+        _emit({"suite": "dflash_block", "target": "qwen3-8b", "draft": "qwen3-8b-shaped, 5 layers", "ctx": ctx,
+               "n": 16, "taps": DFLASH_TAP_LAYERS, "mean_accept": mean, "context_rows": rows,
+               "verify_us": round(us_verify, 1), "context_append_us": round(us_app, 1),
+               "block_draft_us": round(us_block, 1), "cycle_us": round(us_cycle, 1),
+               "tokens_per_cycle": round(toks, 3), "tok_s": round(toks / us_cycle * 1e6, 1)})
+    md.check_error()
+    mt.check_error()
+    mt.close()
+    md.close()
+
+
 def suite_moe(args):
     """DeepSeek-V2-Lite-shaped MoE verify at n = 1..8 with forced synthetic
     routing traces: per-slot vs deduplicated expert reads (time, requested
@@ -820,14 +874,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for counter captures; the line names it)")
-    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "moe", "extras"],
+    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "moe", "extras"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
     if args.suite:
         import __graft_entry__
         __graft_entry__.build()
-        {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash, "moe": suite_moe,
-         "extras": suite_extras}[args.suite](args)
+        {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash,
+         "dflash_block": suite_dflash_block, "moe": suite_moe, "extras": suite_extras}[args.suite](args)
         return
     if args.warmup < 3:
         args.warmup = 3

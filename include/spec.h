@@ -202,6 +202,31 @@ spec_status spec_moe_mode(spec_handle h, int32_t mode);
  * not used while they are on). */
 spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, float* d_out);
 
+/* Block-draft conditioning (mlx-dflash README, "Architecture": the target's
+ * hidden states at chosen layers -> fc -> context features; the draft's
+ * attention is full over the context).  For a handle that serves as the
+ * block draft, with the reading that each of its layers derives the keys and
+ * values of a context position from that position's feature exactly as it
+ * does from a token's residual stream (its input norm, k/v projections, RoPE
+ * at the position):
+ *
+ * spec_set_context_fc: d_fc = bf16 [d_model][n_in * d_model] row-major
+ *   (device, caller-owned, read once and repacked; input index t*d_model + i
+ *   is element i of tap t).  n_in in 1..8.  Once per handle (SPEC_ERR_STATE
+ *   on a second call).  Synchronises the stream.
+ *
+ * spec_context_append: d_taps = fp32 [n_in][16][d_model] (the layout
+ *   spec_set_taps writes), rows 0..m-1 used, m in 1..16, 16-byte aligned.
+ *   feature[r] = fc . bf16(concat_t taps[t][r]) (fp32); then every layer
+ *   writes k/v of positions p..p+m-1 of the TARGET cache (p its length) and
+ *   the length becomes p+m.  Asynchronous on the handle's stream.  Errors:
+ *   SPEC_ERR_STATE (no fc), SPEC_ERR_INVALID_ARG, SPEC_ERR_CAPACITY.
+ * The draft block itself is then an ordinary spec_verify_step of
+ * [last token, mask x 15] on this handle, followed by spec_kv_rollback of
+ * its TARGET cache to p+m. */
+spec_status spec_set_context_fc(spec_handle h, const uint16_t* d_fc, int32_t n_in);
+spec_status spec_context_append(spec_handle h, const float* d_taps, int32_t m);
+
 /* Thread-local description of the last error. */
 const char* spec_last_error(void);
 

@@ -27,7 +27,7 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_check_error", "spec_kv_len", "spec_kv_load", "spec_kv_export", "spec_kv_set_len",
             "spec_moe_force_routing", "spec_last_launch_count", "spec_profile_enable", "spec_profile_read",
             "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds",
-            "spec_set_taps"]
+            "spec_set_taps", "spec_set_context_fc", "spec_context_append"]
 
 
 class SpecError(RuntimeError):
@@ -82,6 +82,8 @@ def library():
         "spec_kv_rollback": [vp, i32, i32],
         "spec_moe_mode": [vp, i32],
         "spec_set_taps": [vp, vp, i32, vp],
+        "spec_set_context_fc": [vp, vp, i32],
+        "spec_context_append": [vp, vp, i32],
         "spec_check_error": [vp],
         "spec_kv_len": [vp, i32, ctypes.POINTER(i32)],
         "spec_kv_load": [vp, i32, i32, vp, vp, i32],
@@ -151,6 +153,14 @@ def spec_set_taps(h, layers, d_out=None):
     (fp32, device).  An empty list switches them off."""
     arr = (ctypes.c_int32 * max(len(layers), 1))(*[int(l) for l in layers])
     _check(library().spec_set_taps(h, arr if layers else None, len(layers), _ptr(d_out)))
+
+
+def spec_set_context_fc(h, d_fc, n_in: int):
+    _check(library().spec_set_context_fc(h, _ptr(d_fc), int(n_in)))
+
+
+def spec_context_append(h, d_taps, m: int):
+    _check(library().spec_context_append(h, _ptr(d_taps), int(m)))
 
 
 def spec_check_error(h):
@@ -339,6 +349,20 @@ class Model:
 
     def moe_mode(self, mode):
         spec_moe_mode(self.h, mode)
+
+    def set_context_fc(self, fc_bits):
+        """Block-draft conditioning: fc as bf16 bits [d_model][n_in*d_model]
+        (host array); uploaded, then repacked by the library."""
+        torch = self._torch
+        n_in = fc_bits.shape[1] // self.cfg.d_model
+        dev = torch.from_numpy(np.ascontiguousarray(fc_bits).view(np.int16)).to("cuda")
+        spec_set_context_fc(self.h, dev, n_in)
+        del dev
+
+    def context_append(self, taps, m):
+        """Append m context positions from tapped hidden states (a device
+        fp32 tensor [n_in][16][d_model], e.g. a target's set_taps buffer)."""
+        spec_context_append(self.h, taps, m)
 
     def set_taps(self, layers):
         """Tap the residual stream after ``layers`` in every verify pass;

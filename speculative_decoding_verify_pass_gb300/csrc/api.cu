@@ -89,6 +89,9 @@ struct spec_model {
     float* route_gates = nullptr;
     int* forced = nullptr;
     bool forced_on = false;
+    PackedMat ctx_fc;                   // block-draft conditioning: fc [d][ctx_n_in*d]
+    int ctx_n_in = 0;
+    uint8_t* xf_ctx = nullptr;          // its operand: the concatenated taps, fp32 fragment order
     std::vector<int> tap_of_layer;      // hidden-state taps: slot of each layer in tap_out, or -1
     float* tap_out = nullptr;           // caller's [count][16][d_model] fp32 buffer
     int tap_count = 0;
@@ -1140,6 +1143,72 @@ spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, f
     h->tap_of_layer = of;
     h->tap_out = count > 0 ? d_out : nullptr;
     h->tap_count = count;
+    return SPEC_OK;
+}
+
+spec_status spec_set_context_fc(spec_handle h, const uint16_t* d_fc, int32_t n_in) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (!d_fc || n_in < 1 || n_in > 8) return fail(SPEC_ERR_INVALID_ARG, "fc must be given for 1..8 tapped layers");
+    if (h->ctx_n_in) return fail(SPEC_ERR_STATE, "the context projection is already set");
+    const int d = h->c.d_model;
+    spec_status s;
+    if ((s = alloc_packed(h, h->ctx_fc, d, n_in * d)) != SPEC_OK) return s;
+    if ((s = pack_into(h, h->ctx_fc, src_rows({d_fc}, {d}, n_in * d, 0))) != SPEC_OK) return s;
+    if ((s = dalloc(h, reinterpret_cast<void**>(&h->xf_ctx), (size_t)n_in * d / kKBlock * kStageX32Bytes)) != SPEC_OK)
+        return s;
+    CU(cudaStreamSynchronize(h->stream));
+    h->ctx_n_in = n_in;
+    return SPEC_OK;
+}
+
+spec_status spec_context_append(spec_handle h, const float* d_taps, int32_t m) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (!h->ctx_n_in) return fail(SPEC_ERR_STATE, "no context projection (spec_set_context_fc)");
+    if (!d_taps || (reinterpret_cast<uintptr_t>(d_taps) & 15)) return fail(SPEC_ERR_INVALID_ARG, "null or unaligned taps");
+    if (m < 1 || m > kMaxBlock) return fail(SPEC_ERR_INVALID_ARG, "m must be in 1..16");
+    spec_status s = check_capacity(h, 0, m);
+    if (s != SPEC_OK) return s;
+    const spec_model_config& c = h->c;
+    const int d = c.d_model, G = h->num_sms;
+    const bool pdl = h->pdl;
+    h->launches = 0;
+    ConcatParams cp{d_taps, h->ctx_n_in, d, h->xf_ctx};
+    CU(launch_concat_taps(cp, h->stream, pdl));
+    ++h->launches;
+    // features = fc . bf16(concatenated taps), fp32 rows into the residual buffer
+    GemmParams p = base_params(h, 0, m);
+    set_mat(h, p, h->ctx_fc, h->xf_ctx, EPI_STORE, G);
+    p.x_f32 = 1;
+    p.y_store = h->x;
+    if ((s = gemm(h, p)) != SPEC_OK) return s;
+    for (int l = 0; l < c.n_layers; ++l) {
+        LayerW& W = h->L[l];
+        RowsParams rp{h->x, m, d, W.attn_norm, h->xf_norm, h->ss};
+        CU(launch_rows_operand(rp, h->stream, pdl));
+        ++h->launches;
+        // this layer's k/v of the context positions; when the q rows fill whole
+        // tiles the GEMM starts at the first k/v tile and never reads them
+        p = base_params(h, 0, m);
+        PackedMat kv = W.qkv;
+        const int qw = c.n_heads * c.head_dim;
+        if (qw % kTileRows == 0) {
+            kv.p = W.qkv.p + (size_t)(qw / kTileRows) * W.qkv.KBs * kStageWBytes;
+            kv.T = W.qkv.T - qw / kTileRows;
+        }
+        set_mat(h, p, kv, h->xf_norm, EPI_QKV, G);
+        p.N = W.qkv.N;
+        if (qw % kTileRows == 0) p.tile0 = qw / kTileRows;
+        p.norm_dim = d;
+        p.rope = h->rope;
+        p.qbuf = h->qbuf;
+        p.kpool = h->kt + h->pool_elems * l;
+        p.vpool = h->vt + h->pool_elems * l;
+        p.block_table = h->block_table;
+        if ((s = gemm(h, p)) != SPEC_OK) return s;
+    }
+    CU(launch_advance(h->st, 0, m, h->stream, pdl));
+    ++h->launches;
+    h->host_len[0] += m;
     return SPEC_OK;
 }
 

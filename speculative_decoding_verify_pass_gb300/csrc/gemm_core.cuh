@@ -161,7 +161,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             if (job >= 64 * p.n) continue;
             const int j = job >> 6, pr = job & 63;
             const int hl = pr / half, i = pr - hl * half;
-            const int R = tile * kTileRows + hl * hd + i;
+            const int R = (tile + p.tile0) * kTileRows + hl * hd + i;
             const int pos = pos0 + j;
             if (R < p.N && R < Nq + Nk) cn[u] = p.rope[(size_t)pos * half + i];
             if (R < p.N && R >= Nq) page[u] = p.block_table[pos / kPageSize];
@@ -173,7 +173,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             const int j = job >> 6, pr = job & 63;
             const int hl = pr / half, i = pr - hl * half;
             const int ra = hl * hd + i, rb = ra + half;
-            const int R = tile * kTileRows + ra;
+            const int R = (tile + p.tile0) * kTileRows + ra;
             if (R >= p.N) continue;
             const float rs = sm.rstd[j];
             float va = cs[ra * kCsLd + j] * rs, vb = cs[rb * kCsLd + j] * rs;

@@ -67,6 +67,7 @@ struct GemmParams {
     float norm_eps;
     // EPI_QKV
     int n_heads, n_kv_heads, head_dim;
+    int tile0;                 // first 128-row tile of the full q|k|v matrix that W starts at (k/v only: q rows skipped)
     const float2* rope;        // [max_pos][head_dim/2] (cos, sin)
     uint16_t* qbuf;            // [16][n_heads*head_dim]
     uint16_t* kpool;           // this layer's pages [page][n_kv_heads][64][head_dim]
@@ -143,6 +144,25 @@ struct CombineParams {           // MoE: x += sum_s gate*y_slot + y_shared
     float* tap;                // optional: the new residual rows, fp32 [16][d] (hidden-state tap)
 };
 cudaError_t launch_moe_combine(const CombineParams& p, cudaStream_t s, bool pdl);
+
+// Block-draft conditioning (context append): the tapped hidden states
+// [n_in][16][d] as one fp32 operand of K = n_in*d (fragment order, gain 1),
+// and fp32 rows [16][d] as a layer's normalised operand (x*gain + sum of
+// squares, as the embedding kernel writes them).
+struct ConcatParams {
+    const float* taps;         // [n_in][16][d]
+    int n_in, d;
+    uint8_t* xf_out;           // [n_in*d/64][4 KB]
+};
+cudaError_t launch_concat_taps(const ConcatParams& p, cudaStream_t s, bool pdl);
+struct RowsParams {
+    float* x;                  // [16][d], rows < n read (and rewritten unchanged)
+    int n, d;
+    const uint16_t* g_next;
+    uint8_t* xf_out;
+    float* ss_out;
+};
+cudaError_t launch_rows_operand(const RowsParams& p, cudaStream_t s, bool pdl);
 
 enum AcceptMode : int { ACC_VERIFY = 0, ACC_DRAFT = 1, ACC_PREFILL = 2 };
 struct AcceptParams {

@@ -68,6 +68,45 @@ __global__ void __launch_bounds__(256) embed_kernel(const __grid_constant__ Embe
     if (rg == 0 && j < p.n) p.ss_out[j * (p.d / kTileRows) + tile] = ssum;
 }
 
+// Tapped hidden states -> one fp32 GEMM operand over K = n_in*d: element
+// (row j, k = t*d + i) = taps[t][j][i].  One CTA per 128 k, 16 threads per
+// row each owning 8 k (which never straddle two taps: d is a multiple of 128).
+__global__ void __launch_bounds__(256) concat_taps_kernel(const __grid_constant__ ConcatParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int j = threadIdx.x >> 4, rg = threadIdx.x & 15;
+    const int k0 = blockIdx.x * kTileRows + rg * 8;
+    const int t = k0 / p.d, i0 = k0 - t * p.d;
+    const float* src = p.taps + ((size_t)t * kMaxBlock + j) * p.d + i0;
+    const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+    const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const int k = k0 + e;
+        *reinterpret_cast<float*>(p.xf_out + (size_t)(k >> 6) * kStageX32Bytes + xfrag32_offset(j, k & 63)) = v[e];
+    }
+}
+
+// Rows x[j] (j < n) as the operand of a normalised GEMM: x*gain and the
+// sum-of-squares partials, exactly as the embedding kernel writes them.
+__global__ void __launch_bounds__(256) rows_operand_kernel(const __grid_constant__ RowsParams p) {
+    pdl_wait();
+    pdl_launch_dependents();
+    const int tile = blockIdx.x, tid = threadIdx.x;
+    const int j = tid >> 4, rg = tid & 15;
+    float ssum = 0.f;
+    if (j < p.n) {
+        const int R0 = tile * kTileRows + rg * 8;
+        float* xr = p.x + (size_t)j * p.d + R0;
+        const float4 a = *reinterpret_cast<const float4*>(xr), b = *reinterpret_cast<const float4*>(xr + 4);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        ssum = store_residual8(xr, v, j, R0, p.g_next, p.xf_out);
+    }
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, o);
+    if (rg == 0 && j < p.n) p.ss_out[j * (p.d / kTileRows) + tile] = ssum;
+}
+
 // MoE layer output: x[j] += sum_s gate[j][s] * y_slot[j][s] + y_shared[j],
 // slots in rank order, then the next norm's operand and sum-of-squares.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant__ CombineParams p) {
@@ -267,6 +306,19 @@ cudaError_t launch_moe_combine(const CombineParams& p, cudaStream_t s, bool pdl)
     CombineParams q = p;
     void* args[] = {&q};
     return launch_ex((const void*)moe_combine_kernel, dim3((unsigned)(p.d / kTileRows)), dim3(256), 0, s, pdl, args);
+}
+
+cudaError_t launch_concat_taps(const ConcatParams& p, cudaStream_t s, bool pdl) {
+    ConcatParams q = p;
+    void* args[] = {&q};
+    return launch_ex((const void*)concat_taps_kernel, dim3((unsigned)(p.n_in * p.d / kTileRows)), dim3(256), 0, s, pdl,
+                     args);
+}
+
+cudaError_t launch_rows_operand(const RowsParams& p, cudaStream_t s, bool pdl) {
+    RowsParams q = p;
+    void* args[] = {&q};
+    return launch_ex((const void*)rows_operand_kernel, dim3((unsigned)(p.d / kTileRows)), dim3(256), 0, s, pdl, args);
 }
 
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s, bool pdl) {

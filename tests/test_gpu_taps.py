@@ -14,7 +14,7 @@ import pytest
 import oracle
 import synth
 from conftest import small_gqa_cfg, small_moe_cfg
-from gpu_common import make_model, torch_cuda
+from gpu_common import ATOL, RTOL, TIE_GAP, make_model, torch_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -150,3 +150,134 @@ def test_taps_graph_and_direct_paths_agree_and_errors(monkeypatch):
         assert not torch.any(taps)
         m.close()
     assert torch.any(out["1"]) and torch.equal(out["1"], out["0"])
+
+
+# ----------------------------------------------------------------------------
+# Block-draft conditioning (context append) and the block pass over it
+# ----------------------------------------------------------------------------
+def _identity_bits(d):
+    eye = np.zeros((d, d), np.uint16)
+    eye[np.arange(d), np.arange(d)] = 0x3F80          # bf16 1.0
+    return eye
+
+
+def test_context_append_of_embeddings_equals_prefill_layer0_bitwise():
+    """fc the identity and taps holding token embeddings: the appended layer-0
+    keys and values are bitwise those the prefill of the same tokens writes
+    (same operand writer, same QKV GEMM)."""
+    torch = torch_cuda()
+    cfg = small_gqa_cfg()
+    w = synth.make_weights(cfg)
+    toks = synth.prompt(cfg, 11, stream=4)
+    a = make_model(cfg, w)
+    a.set_context_fc(_identity_bits(cfg.d_model))
+    taps = torch.zeros((1, 16, cfg.d_model), dtype=torch.float32, device="cuda")
+    taps[0, :11] = torch.from_numpy(synth.bf16_to_f32(w.embed[toks])).to("cuda")
+    a.context_append(taps, 11)
+    a.check_error()
+    assert a.kv_len(0) == 11
+    b = make_model(cfg, w)
+    b.prefill(toks)
+    ka, va = a.kv_export(0, 0, 11)
+    kb, vb = b.kv_export(0, 0, 11)
+    assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    a.close()
+    b.close()
+
+
+@pytest.mark.parametrize("shape", ["gqa-small", "qwen3-8b-2layer"])
+def test_context_append_and_block_pass_match_oracle(shape):
+    """Random fc over three taps; two appends (7 then 9 positions) on top of a
+    synthetic context; every layer's appended keys/values against the oracle's
+    context append, then a block of 16 ([last, mask x 15]) over that cache:
+    logits against the oracle forward on the oracle's cache.  At Qwen3-8B
+    width the reference is the fp64-accumulating oracle and the bound the
+    fp32 oracle's own deviation from it on the same inputs (the floor rule of
+    the full-size tests, computed here rather than stored)."""
+    torch = torch_cuda()
+    from gpu_common import argmax_mismatches, assert_logits_close, assert_within_floor
+    if shape == "gqa-small":
+        cfg = small_gqa_cfg()
+    else:
+        cfg = synth.scaled(synth.PRESETS["qwen3-8b"](max_ctx=256), n_layers=2)
+    w = synth.make_weights(cfg)
+    d, n_in, ctx = cfg.d_model, 3, 70
+    fc = synth.normal_bf16((d, n_in * d), 31, 2)
+    rng = np.random.default_rng(5)
+    m = make_model(cfg, w)
+    m.set_context_fc(fc)
+    orc = oracle.Oracle(cfg, w)
+    oc = orc.new_cache()
+    _load_context(m, orc, oc, cfg, ctx)
+    wide = shape != "gqa-small"
+    if wide:
+        o64 = oracle.Oracle(cfg, w, acc64=True)
+        oc64 = o64.new_cache()
+        for l in range(cfg.n_layers):
+            oc64.load(l, synth.synthetic_kv(cfg, l, ctx, 0).reshape(ctx, -1),
+                      synth.synthetic_kv(cfg, l, ctx, 1).reshape(ctx, -1))
+        oc64.set_len(ctx)
+    for rows in (7, 9):
+        taps = rng.standard_normal((n_in, 16, d)).astype(np.float32)
+        m.context_append(torch.from_numpy(taps).to("cuda"), rows)
+        orc.context_append(oc, fc, taps, rows)
+        if wide:
+            o64.context_append(oc64, fc, taps, rows)
+    m.check_error()
+    total = ctx + 16
+    assert m.kv_len(0) == total and oc.len == total
+    for l in range(cfg.n_layers):
+        kg, vg = m.kv_export(0, l, total)
+        for which, g in ((0, kg), (1, vg)):
+            got = synth.bf16_to_f32(g.reshape(total, -1)[ctx:]).astype(np.float64)
+            ref = oc.read(l, which, total)[ctx:].astype(np.float64)
+            err = np.abs(got - ref)
+            scale = float(np.max(np.abs(ref)))
+            assert np.max(err) <= 2e-2 * scale and np.mean(err) <= 2e-3 * scale, (shape, l, which)
+    mask = cfg.vocab - 1
+    block = [int(synth.prompt(cfg, 1, stream=9)[0])] + [mask] * 15
+    am, _, lg, _ = m.verify(torch.tensor(block, dtype=torch.int32, device="cuda"), logits=True)
+    m.check_error()
+    ref, _, _ = orc.forward(oc, orc.full_plan, block, total)
+    if wide:
+        ref64, _, _ = o64.forward(oc64, o64.full_plan, block, total)
+        e = np.abs(ref.astype(np.float64) - ref64)
+        floor = dict(mean=float(e.mean()), max=float(e.max()),
+                     share=float(np.mean(e > ATOL + RTOL * np.abs(ref64))))
+        assert_within_floor(lg.cpu().numpy(), ref64, floor, "block pass %s" % shape)
+        # a near tie is a top-two margin the fp32 arithmetic itself may reorder
+        argmax_mismatches(am.cpu().numpy(), ref64, tie_gap=max(TIE_GAP, 2.0 * floor["max"]))
+    else:
+        assert_logits_close(lg.cpu().numpy(), ref, "block pass %s" % shape)
+        argmax_mismatches(am.cpu().numpy(), ref)
+    m.rollback(0, total)                   # the block's own keys/values are dropped
+    assert m.kv_len(0) == total
+    m.close()
+
+
+def test_context_append_errors():
+    torch = torch_cuda()
+    import speculative_decoding_verify_pass_gb300 as sv
+    cfg = small_gqa_cfg()
+    w = synth.make_weights(cfg)
+    m = make_model(cfg, w)
+    taps = torch.zeros((2, 16, cfg.d_model), dtype=torch.float32, device="cuda")
+    with pytest.raises(sv.SpecError) as e:
+        m.context_append(taps, 4)                      # no fc yet
+    assert e.value.status == sv.SPEC_ERR_STATE
+    m.set_context_fc(synth.normal_bf16((cfg.d_model, 2 * cfg.d_model), 3, 1))
+    with pytest.raises(sv.SpecError) as e:
+        m.set_context_fc(synth.normal_bf16((cfg.d_model, 2 * cfg.d_model), 3, 1))
+    assert e.value.status == sv.SPEC_ERR_STATE
+    for bad in (0, 17):
+        with pytest.raises(sv.SpecError) as e:
+            m.context_append(taps, bad)
+        assert e.value.status == sv.SPEC_ERR_INVALID_ARG
+    m.kv_set_len(0, cfg.max_ctx - 3)
+    with pytest.raises(sv.SpecError) as e:
+        m.context_append(taps, 4)
+    assert e.value.status == sv.SPEC_ERR_CAPACITY
+    m.context_append(taps, 3)
+    m.check_error()
+    assert m.kv_len(0) == cfg.max_ctx
+    m.close()
