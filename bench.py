@@ -730,6 +730,47 @@ def suite_dflash_block(args):
     md.close()
 
 
+def suite_batch(args):
+    """Batched sequences: one verify pass over the blocks of nseq independent
+    Qwen3-4B sequences at context 2048 (each its own synthetic cache), for
+    nseq * n = 16 rows and for n = 4 at nseq = 1, 2, 4.  Weights are read once
+    per pass for all sequences; each sequence adds its own KV reads."""
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    ctx, reps = 2048, 10
+    cfg = synth.qwen3_4b(max_ctx=ctx + 16 * (reps + 4))
+    w = synth.make_weights(cfg)
+    m = sv.Model(cfg, w)
+    m.batch_reserve(16)
+    for l in range(cfg.n_layers):
+        k = synth.synthetic_kv(cfg, l, ctx, 0)
+        v = synth.synthetic_kv(cfg, l, ctx, 1)
+        for q in range(16):
+            m.batch_kv_load(q, l, k, v)
+    kv_row = 2 * cfg.n_kv_heads * cfg.head_dim * 2
+    for nseq, n in ((1, 16), (2, 8), (4, 4), (8, 2), (16, 1), (1, 4), (2, 4)):
+        for q in range(nseq):
+            m.batch_set_len(q, ctx)
+        blocks = torch.tensor([synth.prompt(cfg, n, stream=q).tolist() for q in range(nseq)], dtype=torch.int32,
+                              device="cuda")
+        am = torch.empty((nseq, n), dtype=torch.int32, device="cuda")
+        acc = torch.empty(nseq, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            sv.spec_verify_batch(m.h, blocks, am, acc)
+        for q in range(nseq):
+            m.batch_set_len(q, ctx)
+        us = _time_calls(torch, lambda: sv.spec_verify_batch(m.h, blocks, am, acc), reps, warm=0)
+        b = stepmodel.pass_bytes(cfg, nseq * n, ctx) + (nseq - 1) * cfg.n_layers * kv_row * ctx
+        _emit({"suite": "batch", "config": "qwen3-4b", "ctx": ctx, "nseq": nseq, "n": n, "rows": nseq * n,
+               "pass_us": round(us, 1), "bytes": b, "GBps": round(b / us / 1e3, 1),
+               "frac_measured_peak": round(b / us / 1e3 / measured_peaks()[0], 3),
+               "sequences_per_s": round(nseq / us * 1e6, 1), "rows_per_s": round(nseq * n / us * 1e6, 1)})
+    m.check_error()
+    m.close()
+
+
 def suite_moe(args):
     """DeepSeek-V2-Lite-shaped MoE verify at n = 1..8 with forced synthetic
     routing traces: per-slot vs deduplicated expert reads (time, requested
@@ -874,14 +915,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for counter captures; the line names it)")
-    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "moe", "extras"],
+    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "batch", "moe", "extras"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
     if args.suite:
         import __graft_entry__
         __graft_entry__.build()
         {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash,
-         "dflash_block": suite_dflash_block, "moe": suite_moe, "extras": suite_extras}[args.suite](args)
+         "dflash_block": suite_dflash_block, "batch": suite_batch, "moe": suite_moe,
+         "extras": suite_extras}[args.suite](args)
         return
     if args.warmup < 3:
         args.warmup = 3

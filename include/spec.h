@@ -227,6 +227,35 @@ spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, f
 spec_status spec_set_context_fc(spec_handle h, const uint16_t* d_fc, int32_t n_in);
 spec_status spec_context_append(spec_handle h, const float* d_taps, int32_t m);
 
+/* Batched sequences (next row NEXT-3; the pages name several sequences per
+ * pass as a way to raise flops per weight byte).  One pass verifies the
+ * blocks of nseq independent sequences: every weight is read once for all
+ * nseq * n rows, while each sequence attends only to its own cache.
+ *
+ * spec_batch_reserve: allocates target caches for nseq (1..16) sequences of
+ *   max_ctx positions each, next to the handle's own caches.  Once per
+ *   handle (SPEC_ERR_STATE on a second call).  Synchronises the stream.
+ * spec_batch_kv_load / spec_batch_kv_export: as spec_kv_load/export, for
+ *   sequence `seq` (0..reserved-1) and layer `slot`.
+ * spec_batch_set_len: sets sequence seq's length (synchronises the stream).
+ * spec_batch_len: synchronises and returns sequence seq's device length.
+ * spec_verify_batch: d_blocks = int32 [nseq][n] (sequence q's block: its
+ *   last accepted token then n-1 drafts, at positions len_q .. len_q+n-1),
+ *   nseq * n <= 16.  Outputs d_argmax [nseq][n], d_accept [nseq] (the greedy
+ *   cumulative-product rule per sequence), d_logits_opt NULL or
+ *   [nseq*n][vocab].  Each sequence's length then becomes len_q + accept_q + 1
+ *   on the device (the rollback rule of spec_kv_rollback, applied here).
+ *   Row j of sequence q is bitwise the row a single-sequence verify of the
+ *   same block on the same cache gives.  Errors: SPEC_ERR_INVALID_ARG,
+ *   SPEC_ERR_CAPACITY; state unchanged. */
+spec_status spec_batch_reserve(spec_handle h, int32_t nseq);
+spec_status spec_batch_kv_load(spec_handle h, int32_t seq, int32_t slot, const void* d_k, const void* d_v, int32_t ctx);
+spec_status spec_batch_kv_export(spec_handle h, int32_t seq, int32_t slot, void* d_k, void* d_v, int32_t ctx);
+spec_status spec_batch_set_len(spec_handle h, int32_t seq, int32_t len);
+spec_status spec_batch_len(spec_handle h, int32_t seq, int32_t* out_len);
+spec_status spec_verify_batch(spec_handle h, const int32_t* d_blocks, int32_t nseq, int32_t n, int32_t* d_argmax,
+                              int32_t* d_accept, float* d_logits_opt);
+
 /* Thread-local description of the last error. */
 const char* spec_last_error(void);
 

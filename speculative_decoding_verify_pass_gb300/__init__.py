@@ -27,7 +27,9 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_check_error", "spec_kv_len", "spec_kv_load", "spec_kv_export", "spec_kv_set_len",
             "spec_moe_force_routing", "spec_last_launch_count", "spec_profile_enable", "spec_profile_read",
             "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds",
-            "spec_set_taps", "spec_set_context_fc", "spec_context_append"]
+            "spec_set_taps", "spec_set_context_fc", "spec_context_append", "spec_batch_reserve",
+            "spec_batch_kv_load", "spec_batch_kv_export", "spec_batch_set_len", "spec_batch_len",
+            "spec_verify_batch"]
 
 
 class SpecError(RuntimeError):
@@ -83,6 +85,12 @@ def library():
         "spec_moe_mode": [vp, i32],
         "spec_set_taps": [vp, vp, i32, vp],
         "spec_set_context_fc": [vp, vp, i32],
+        "spec_batch_reserve": [vp, i32],
+        "spec_batch_kv_load": [vp, i32, i32, vp, vp, i32],
+        "spec_batch_kv_export": [vp, i32, i32, vp, vp, i32],
+        "spec_batch_set_len": [vp, i32, i32],
+        "spec_batch_len": [vp, i32, vp],
+        "spec_verify_batch": [vp, vp, i32, i32, vp, vp, vp],
         "spec_context_append": [vp, vp, i32],
         "spec_check_error": [vp],
         "spec_kv_len": [vp, i32, ctypes.POINTER(i32)],
@@ -161,6 +169,34 @@ def spec_set_context_fc(h, d_fc, n_in: int):
 
 def spec_context_append(h, d_taps, m: int):
     _check(library().spec_context_append(h, _ptr(d_taps), int(m)))
+
+
+def spec_batch_reserve(h, nseq: int):
+    _check(library().spec_batch_reserve(h, int(nseq)))
+
+
+def spec_batch_kv_load(h, seq, slot, d_k, d_v, ctx):
+    _check(library().spec_batch_kv_load(h, int(seq), int(slot), _ptr(d_k), _ptr(d_v), int(ctx)))
+
+
+def spec_batch_kv_export(h, seq, slot, d_k, d_v, ctx):
+    _check(library().spec_batch_kv_export(h, int(seq), int(slot), _ptr(d_k), _ptr(d_v), int(ctx)))
+
+
+def spec_batch_set_len(h, seq: int, length: int):
+    _check(library().spec_batch_set_len(h, int(seq), int(length)))
+
+
+def spec_batch_len(h, seq: int) -> int:
+    out = ctypes.c_int32(0)
+    _check(library().spec_batch_len(h, int(seq), ctypes.byref(out)))
+    return int(out.value)
+
+
+def spec_verify_batch(h, d_blocks, d_argmax, d_accept, d_logits=None):
+    """d_blocks: int32 device tensor [nseq][n]."""
+    nseq, n = int(d_blocks.shape[0]), int(d_blocks.shape[1])
+    _check(library().spec_verify_batch(h, _ptr(d_blocks), nseq, n, _ptr(d_argmax), _ptr(d_accept), _ptr(d_logits)))
 
 
 def spec_check_error(h):
@@ -363,6 +399,41 @@ class Model:
         """Append m context positions from tapped hidden states (a device
         fp32 tensor [n_in][16][d_model], e.g. a target's set_taps buffer)."""
         spec_context_append(self.h, taps, m)
+
+    def batch_reserve(self, nseq):
+        spec_batch_reserve(self.h, nseq)
+
+    def batch_kv_load(self, seq, slot, k_bits, v_bits):
+        torch = self._torch
+        k = torch.from_numpy(np.ascontiguousarray(k_bits).view(np.int16)).to("cuda")
+        v = torch.from_numpy(np.ascontiguousarray(v_bits).view(np.int16)).to("cuda")
+        spec_batch_kv_load(self.h, seq, slot, k, v, k_bits.shape[0])
+        torch.cuda.synchronize()
+
+    def batch_kv_export(self, seq, slot, ctx):
+        c = self.cfg
+        k = self._torch.empty((ctx, c.n_kv_heads, c.head_dim), dtype=self._torch.int16, device="cuda")
+        v = self._torch.empty_like(k)
+        spec_batch_kv_export(self.h, seq, slot, k, v, ctx)
+        self._torch.cuda.synchronize()
+        return k.cpu().numpy().view(np.uint16), v.cpu().numpy().view(np.uint16)
+
+    def batch_set_len(self, seq, length):
+        spec_batch_set_len(self.h, seq, length)
+
+    def batch_len(self, seq):
+        return spec_batch_len(self.h, seq)
+
+    def verify_batch(self, d_blocks, logits=False):
+        """d_blocks: int32 device tensor [nseq][n]; returns (argmax [nseq][n],
+        accept [nseq], logits [nseq*n][V] or None)."""
+        torch = self._torch
+        nseq, n = d_blocks.shape
+        am = torch.empty((nseq, n), dtype=torch.int32, device="cuda")
+        acc = torch.empty(nseq, dtype=torch.int32, device="cuda")
+        lg = torch.empty((nseq * n, self.cfg.vocab), dtype=torch.float32, device="cuda") if logits else None
+        spec_verify_batch(self.h, d_blocks, am, acc, lg)
+        return am, acc, lg
 
     def set_taps(self, layers):
         """Tap the residual stream after ``layers`` in every verify pass;

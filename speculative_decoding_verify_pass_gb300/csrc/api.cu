@@ -89,6 +89,15 @@ struct spec_model {
     float* route_gates = nullptr;
     int* forced = nullptr;
     bool forced_on = false;
+    // batched sequences (spec_batch_reserve): target caches of their own
+    int bat_cap = 0;                    // sequences reserved
+    uint16_t *kb = nullptr, *vb = nullptr;   // [layer][bat_cap * max_pages pages][Hkv][64][hd]
+    int* bt_b = nullptr;                // identity table over bat_cap * max_pages pages
+    int* seq_len = nullptr;             // device [16]
+    std::vector<int> bat_host_len;      // upper bounds of the device lengths
+    float* battn_o = nullptr;           // attention partials of all sequences
+    float2* battn_ml = nullptr;
+    int bat_nseq = 0;                   // > 0 while a batched pass is built
     PackedMat ctx_fc;                   // block-draft conditioning: fc [d][ctx_n_in*d]
     int ctx_n_in = 0;
     uint8_t* xf_ctx = nullptr;          // its operand: the concatenated taps, fp32 fragment order
@@ -391,7 +400,7 @@ void clear_graphs(spec_model* h) {
 spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
                      int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair, int32_t* d_token,
                      const int32_t* d_block) {
-    if (h->use_pass && h->c.n_experts == 0 && h->tap_count == 0)
+    if (h->use_pass && h->c.n_experts == 0 && h->tap_count == 0 && h->bat_nseq == 0)
         return run_pass_kernel(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_pair, d_token, d_block);
     if (h->trace) {  // a traced pass runs its launches directly, each with its own stamp slots
         h->trace_mode = 2;
@@ -407,7 +416,7 @@ spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, P
                                         (uintptr_t)d_argmax, (uintptr_t)d_accept, (uintptr_t)d_logits,
                                         (uintptr_t)d_ids, (uintptr_t)d_pair, (uintptr_t)d_token, (uintptr_t)d_block,
                                         (uintptr_t)h->moe_mode, (uintptr_t)h->forced_on, (uintptr_t)h->tap_out,
-                                        (uintptr_t)h->tap_count};
+                                        (uintptr_t)h->tap_count, (uintptr_t)h->bat_nseq};
     auto f = h->graphs.find(key);
     if (f == h->graphs.end()) {
         if (h->graphs.size() >= 256) clear_graphs(h);
@@ -473,6 +482,12 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
                          : nullptr;
         uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
         uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
+        const bool bat = h->bat_nseq > 0;   // batched sequences: their own caches, positions and pages
+        const int rps = bat ? n / h->bat_nseq : n;
+        if (bat) {
+            kpool = h->kb + h->pool_elems * h->bat_cap * l;
+            vpool = h->vb + h->pool_elems * h->bat_cap * l;
+        }
 
         // QKV (attn RMSNorm scale, RoPE, paged KV append)
         GemmParams p = base_params(h, which, n);
@@ -482,20 +497,30 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         p.qbuf = h->qbuf;
         p.kpool = kpool;
         p.vpool = vpool;
-        p.block_table = h->block_table;
+        p.block_table = bat ? h->bt_b : h->block_table;
+        if (bat) {
+            p.seq_len = h->seq_len;
+            p.rows_per_seq = rps;
+            p.seq_pages = h->max_pages;
+        }
         if ((s = gemm(h, p)) != SPEC_OK) return s;
 
         AttnParams a{};
         a.qbuf = h->qbuf;
         a.kpool = kpool;
         a.vpool = vpool;
-        a.block_table = h->block_table;
-        a.part_o = h->attn_o;
-        a.part_ml = h->attn_ml;
+        a.block_table = bat ? h->bt_b : h->block_table;
+        a.part_o = bat ? h->battn_o : h->attn_o;
+        a.part_ml = bat ? h->battn_ml : h->attn_ml;
         a.xf_out = h->xf_o;
         a.st = h->st;
         a.which = which;
-        a.n = n;
+        a.n = rps;
+        if (bat) {
+            a.seq_len = h->seq_len;
+            a.nseq = h->bat_nseq;
+            a.seq_pages = h->max_pages;
+        }
         a.n_heads = c.n_heads;
         a.n_kv_heads = c.n_kv_heads;
         a.head_dim = hd;
@@ -613,6 +638,11 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
     ap.out_accept = d_accept;
     ap.out_pair = d_pair;
     ap.out_token = d_token;
+    if (h->bat_nseq > 0) {
+        ap.mode = ACC_BATCH;
+        ap.seq_len = h->seq_len;
+        ap.nseq = h->bat_nseq;
+    }
     CU(launch_accept(ap, h->stream, pdl));
     ++h->launches;
     return SPEC_OK;
@@ -1144,6 +1174,101 @@ spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, f
     h->tap_out = count > 0 ? d_out : nullptr;
     h->tap_count = count;
     return SPEC_OK;
+}
+
+spec_status spec_batch_reserve(spec_handle h, int32_t nseq) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (nseq < 1 || nseq > kMaxBlock) return fail(SPEC_ERR_INVALID_ARG, "nseq must be in 1..16");
+    if (h->bat_cap) return fail(SPEC_ERR_STATE, "batch caches are already reserved");
+    const spec_model_config& c = h->c;
+    const size_t pages = (size_t)nseq * h->max_pages;
+    const size_t parts = (size_t)nseq * c.n_kv_heads * h->nch * 64;
+    spec_status s;
+    if ((s = dalloc_t(h, &h->kb, h->pool_elems * nseq * c.n_layers)) != SPEC_OK) return s;
+    if ((s = dalloc_t(h, &h->vb, h->pool_elems * nseq * c.n_layers)) != SPEC_OK) return s;
+    if ((s = dalloc_t(h, &h->bt_b, pages)) != SPEC_OK) return s;
+    if ((s = dalloc_t(h, &h->seq_len, (size_t)kMaxBlock)) != SPEC_OK) return s;
+    if ((s = dalloc_t(h, &h->battn_o, parts * c.head_dim)) != SPEC_OK) return s;
+    if ((s = dalloc_t(h, &h->battn_ml, parts)) != SPEC_OK) return s;
+    std::vector<int> bt(pages);
+    for (size_t i = 0; i < pages; ++i) bt[i] = (int)i;
+    CU(cudaMemcpyAsync(h->bt_b, bt.data(), sizeof(int) * bt.size(), cudaMemcpyHostToDevice, h->stream));
+    CU(cudaStreamSynchronize(h->stream));
+    h->bat_cap = nseq;
+    h->bat_host_len.assign(nseq, 0);
+    return SPEC_OK;
+}
+
+static spec_status batch_kv_io(spec_handle h, int32_t seq, int32_t slot, void* dk, void* dv, int32_t ctx, bool load) {
+    if (!h || !dk || !dv) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (seq < 0 || seq >= h->bat_cap) return fail(SPEC_ERR_INVALID_ARG, "sequence %d not reserved", seq);
+    if (slot < 0 || slot >= h->c.n_layers) return fail(SPEC_ERR_INVALID_ARG, "slot %d out of range", slot);
+    if (ctx < 0 || ctx > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "ctx %d out of range", ctx);
+    const size_t off = h->pool_elems * ((size_t)h->bat_cap * slot + seq);   // the sequence's own pages
+    CU(launch_kv_io(h->kb + off, h->block_table, static_cast<uint16_t*>(dk), ctx, h->c.n_kv_heads, h->c.head_dim, load,
+                    h->stream));
+    CU(launch_kv_io(h->vb + off, h->block_table, static_cast<uint16_t*>(dv), ctx, h->c.n_kv_heads, h->c.head_dim, load,
+                    h->stream));
+    return SPEC_OK;
+}
+
+spec_status spec_batch_kv_load(spec_handle h, int32_t seq, int32_t slot, const void* d_k, const void* d_v, int32_t ctx) {
+    return batch_kv_io(h, seq, slot, const_cast<void*>(d_k), const_cast<void*>(d_v), ctx, true);
+}
+
+spec_status spec_batch_kv_export(spec_handle h, int32_t seq, int32_t slot, void* d_k, void* d_v, int32_t ctx) {
+    return batch_kv_io(h, seq, slot, d_k, d_v, ctx, false);
+}
+
+spec_status spec_batch_set_len(spec_handle h, int32_t seq, int32_t len) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (seq < 0 || seq >= h->bat_cap) return fail(SPEC_ERR_INVALID_ARG, "sequence %d not reserved", seq);
+    if (len < 0 || len > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "length %d out of range", len);
+    const int32_t v = len;
+    CU(cudaMemcpyAsync(h->seq_len + seq, &v, sizeof(v), cudaMemcpyHostToDevice, h->stream));
+    CU(cudaStreamSynchronize(h->stream));
+    h->bat_host_len[seq] = len;
+    return SPEC_OK;
+}
+
+spec_status spec_batch_len(spec_handle h, int32_t seq, int32_t* out_len) {
+    if (!h || !out_len) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (seq < 0 || seq >= h->bat_cap) return fail(SPEC_ERR_INVALID_ARG, "sequence %d not reserved", seq);
+    CU(cudaStreamSynchronize(h->stream));
+    int32_t v = 0;
+    CU(cudaMemcpy(&v, h->seq_len + seq, sizeof(v), cudaMemcpyDeviceToHost));
+    h->bat_host_len[seq] = v;
+    *out_len = v;
+    return SPEC_OK;
+}
+
+spec_status spec_verify_batch(spec_handle h, const int32_t* d_blocks, int32_t nseq, int32_t n, int32_t* d_argmax,
+                              int32_t* d_accept, float* d_logits_opt) {
+    if (!h || !d_blocks || !d_argmax || !d_accept) return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (nseq < 1 || nseq > h->bat_cap) return fail(SPEC_ERR_INVALID_ARG, "nseq %d outside the %d reserved", nseq, h->bat_cap);
+    if (n < 1 || nseq * n > kMaxBlock) return fail(SPEC_ERR_INVALID_ARG, "nseq * n must be in 1..16");
+    bool synced = false;
+    for (int q = 0; q < nseq; ++q) {
+        if (h->bat_host_len[q] + n <= h->c.max_ctx) continue;
+        if (!synced) {   // the host's bounds may be stale after device-side accepts
+            CU(cudaStreamSynchronize(h->stream));
+            std::vector<int32_t> lens(h->bat_cap);
+            CU(cudaMemcpy(lens.data(), h->seq_len, sizeof(int32_t) * h->bat_cap, cudaMemcpyDeviceToHost));
+            for (int t = 0; t < h->bat_cap; ++t) h->bat_host_len[t] = lens[t];
+            synced = true;
+        }
+        if (h->bat_host_len[q] + n > h->c.max_ctx)
+            return fail(SPEC_ERR_CAPACITY, "sequence %d holds %d positions; %d more exceed max_ctx %d", q,
+                        h->bat_host_len[q], n, h->c.max_ctx);
+    }
+    h->launches = 0;
+    h->bat_nseq = nseq;
+    spec_status s = run_pass(h, 0, d_blocks, nseq * n, PASS_VERIFY, d_argmax, d_accept, d_logits_opt, nullptr, nullptr,
+                             nullptr, d_blocks);
+    h->bat_nseq = 0;
+    if (s == SPEC_OK)
+        for (int q = 0; q < nseq; ++q) h->bat_host_len[q] += n;
+    return s;
 }
 
 spec_status spec_set_context_fc(spec_handle h, const uint16_t* d_fc, int32_t n_in) {

@@ -35,17 +35,18 @@ __global__ void __maxnreg__(192) attn_partial_kernel(const __grid_constant__ Att
     uint16_t* svv = sk + kAttnChunk * HD;
     __shared__ uint64_t bar;
 
-    const int h = blockIdx.x, chunk = blockIdx.y;
+    const int h = blockIdx.x, chunk = blockIdx.y, sq = blockIdx.z;   // sq: sequence (batched passes)
     const int tid = threadIdx.x;
-    const int cta = chunk * gridDim.x + h;
+    const int cta = (sq * gridDim.y + chunk) * gridDim.x + h;
     long long* tr = (p.trace && cta < kTraceCtas && tid == 0) ? p.trace + (size_t)cta * 4 : nullptr;
     if (tr) tr[0] = trace_clock();
     // The cache length and the keys/values of positions before it were
     // written by kernels that completed before the preceding QKV kernel
     // passed its own dependency wait, so they may be read before ours; only
     // the block's new rows (positions >= pos0) come from the QKV kernel.
-    const int pos0 = p.st->len[p.which];
+    const int pos0 = p.seq_len ? p.seq_len[sq] : p.st->len[p.which];
     const int total = pos0 + p.n;
+    const int* btab = p.block_table + (p.seq_len ? sq * p.seq_pages : 0);
     const int start = chunk * kAttnChunk;
     if (start >= total || total > p.nch * kAttnChunk) {
         pdl_wait();
@@ -56,7 +57,7 @@ __global__ void __maxnreg__(192) attn_partial_kernel(const __grid_constant__ Att
     }
     constexpr uint32_t kSlab = kPageSize * HD * 2;
     auto issue = [&](int pg) {
-        const int page = p.block_table[start / kPageSize + pg];
+        const int page = btab[start / kPageSize + pg];
         const size_t off = ((size_t)(page * p.n_kv_heads + h) * kPageSize) * HD;
         bulk_g2s(sk + pg * kPageSize * HD, p.kpool + off, kSlab, &bar);
         bulk_g2s(svv + pg * kPageSize * HD, p.vpool + off, kSlab, &bar);
@@ -78,14 +79,17 @@ __global__ void __maxnreg__(192) attn_partial_kernel(const __grid_constant__ Att
     float* scratch = reinterpret_cast<float*>(smem_raw + 2 * kAttnChunk * HD * 2);
     uint16_t* qs = reinterpret_cast<uint16_t*>(smem_raw + 2 * kAttnChunk * HD * 2 + attn_core::kAttnScratchBytes);
     const int G = p.n_heads / p.n_kv_heads, R = p.n * G;
+    const uint16_t* qsrc = p.qbuf + (size_t)sq * p.n * p.n_heads * HD;   // this sequence's query rows
     for (int c = tid; c < R * (HD / 8); c += kAttnThreads) {
         const int r = c / (HD / 8), q = c % (HD / 8);
         cp_async16(qs + r * attn_core::q_stride<HD>() + q * 8,
-                   p.qbuf + ((size_t)(r / G) * p.n_heads + h * G + r % G) * HD + q * 8);
+                   qsrc + ((size_t)(r / G) * p.n_heads + h * G + r % G) * HD + q * 8);
     }
     cp_async_wait_all();
     __syncthreads();
-    attn_core::attn_unit<HD>(p, sk, sk + kPageSize * HD, svv, svv + kPageSize * HD, scratch, qs, 4, h, chunk, pos0, tid,
+    const size_t seq_base = (size_t)sq * p.n_kv_heads * p.nch * 64;
+    attn_core::attn_unit<HD>(p, sk, sk + kPageSize * HD, svv, svv + kPageSize * HD, scratch, qs, 4, h, chunk, pos0, p.n,
+                             seq_base, tid,
                              [&] {
                                  mbar_wait(&bar, 0, &p.st->error, 3);
                                  if (tr) tr[2] = trace_clock();
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(attn_core::kAttnCombThreads) attn_combine_kern
     pdl_wait();
     pdl_launch_dependents();
     if (tr) tr[1] = trace_clock();
-    const int total = p.st->len[p.which] + p.n;
+    const int total = p.st->len[p.which] + p.n;   // batched passes: per sequence, in comb_rows
     int nc = (total + kAttnChunk - 1) / kAttnChunk;
     if (nc > p.nch) nc = p.nch;
     constexpr int kWarps = attn_core::kAttnCombThreads / 32;
@@ -146,7 +150,9 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t s, bool pdl) {
     AttnParams q = p;
     void* args[] = {&q};
     cudaError_t e;
-    const dim3 g1((unsigned)p.n_kv_heads, (unsigned)p.nch), g2((unsigned)((p.n_heads * p.n + attn_core::kAttnCombThreads / 32 - 1) / (attn_core::kAttnCombThreads / 32)));
+    const int nseq = p.seq_len ? p.nseq : 1;
+    const dim3 g1((unsigned)p.n_kv_heads, (unsigned)p.nch, (unsigned)nseq);
+    const dim3 g2((unsigned)((nseq * p.n_heads * p.n + attn_core::kAttnCombThreads / 32 - 1) / (attn_core::kAttnCombThreads / 32)));
     if (p.head_dim == 128)
         e = launch_pdl((const void*)attn_partial_kernel<128>, g1, dim3(kAttnThreads), attn_smem(128), s, pdl, args);
     else if (p.head_dim == 64)

@@ -53,8 +53,8 @@ __host__ __device__ constexpr int q_stride() { return HD + 8; }
 template <int HD, int C, class WaitSlabs>
 __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t* sk0, const uint16_t* sk1,
                                             const uint16_t* sv0, const uint16_t* sv1, float* scratch,
-                                            const uint16_t* qs, int h, int chunk, int pos0, int tid,
-                                            WaitSlabs& wait_slabs) {
+                                            const uint16_t* qs, int h, int chunk, int pos0, int n, size_t seq_base,
+                                            int tid, WaitSlabs& wait_slabs) {
     constexpr int kTiles = HD / 16;                                   // dim tiles
     constexpr int par = 8 / C;                                        // row groups at once
     constexpr int kgs = 8 / C;                                        // key groups per warp
@@ -62,14 +62,14 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, cc = lane & 3;
     const int G = a.n_heads / a.n_kv_heads;
-    const int R = a.n * G;
+    const int R = n * G;
     const int nrg = (R + 15) / 16;
     const int slot = warp / C, sub = warp % C;
     float* smax = scratch + slot * (kAttnSlotBytes / 4);              // [8][16]
     float* ssum = smax + 128;                                         // [8][16]
     uint32_t* pf = reinterpret_cast<uint32_t*>(smax + 256);           // [8][32][8]
     const float k2 = a.scale_log2;
-    const size_t base = ((size_t)h * a.nch + chunk) * 64;
+    const size_t base = seq_base + ((size_t)h * a.nch + chunk) * 64;
     // barrier of the C warps sharing a slot (the whole CTA when C = 8)
     auto slot_sync = [&] {
         if (C == 8)
@@ -255,15 +255,15 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
 template <int HD, class WaitSlabs>
 __device__ __forceinline__ void attn_unit(const AttnParams& a, const uint16_t* sk0, const uint16_t* sk1,
                                           const uint16_t* sv0, const uint16_t* sv1, float* scratch,
-                                          const uint16_t* qs, int slots, int h, int chunk, int pos0, int tid,
-                                          WaitSlabs wait_slabs) {
-    const int nrg = (a.n * (a.n_heads / a.n_kv_heads) + 15) / 16;
+                                          const uint16_t* qs, int slots, int h, int chunk, int pos0, int n,
+                                          size_t seq_base, int tid, WaitSlabs wait_slabs) {
+    const int nrg = (n * (a.n_heads / a.n_kv_heads) + 15) / 16;
     if (slots <= 1 || nrg <= 1)
-        attn_unit_c<HD, 8>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, tid, wait_slabs);
+        attn_unit_c<HD, 8>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, n, seq_base, tid, wait_slabs);
     else if (nrg <= 2)
-        attn_unit_c<HD, 4>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, tid, wait_slabs);
+        attn_unit_c<HD, 4>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, n, seq_base, tid, wait_slabs);
     else
-        attn_unit_c<HD, 2>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, tid, wait_slabs);
+        attn_unit_c<HD, 2>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, n, seq_base, tid, wait_slabs);
 }
 
 // Rows (query head, token) u0, u0+ustep, ...: one warp per row merges the nc
@@ -279,13 +279,23 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
     constexpr int V = HD / 32;   // dimensions per lane: 4 (hd 128) or 2 (hd 64)
     constexpr int kFirst = 24;
     const int G = a.n_heads / a.n_kv_heads;
-    const int U = a.n_heads * a.n;
+    const int nseq = a.seq_len ? a.nseq : 1;
+    const int per = a.n_heads * a.n;            // rows of one sequence
+    const int U = per * nseq;
     const size_t cstride = (size_t)64 * HD;
     for (int u = u0; u < U; u += ustep) {
-        const int qh = u % a.n_heads, j = u / a.n_heads;
-        const int h = qh / G, r = j * G + qh % G;
-        const float2* ml = a.part_ml + (size_t)h * a.nch * 64 + r;
-        const float* po = a.part_o + ((size_t)h * a.nch * 64 + r) * HD + lane * V;
+        const int sq = u / per, uu = u - sq * per;
+        const int qh = uu % a.n_heads, jl = uu / a.n_heads;
+        const int j = sq * a.n + jl;              // the row of the pass
+        if (a.seq_len) {                          // this sequence's own chunk count
+            const int tot = a.seq_len[sq] + a.n;
+            nc = (tot + kAttnChunk - 1) / kAttnChunk;
+            if (nc > a.nch) nc = a.nch;
+        }
+        const int h = qh / G, r = jl * G + qh % G;
+        const size_t sbase = (size_t)sq * a.n_kv_heads * a.nch * 64;
+        const float2* ml = a.part_ml + sbase + (size_t)h * a.nch * 64 + r;
+        const float* po = a.part_o + (sbase + (size_t)h * a.nch * 64 + r) * HD + lane * V;
         float ob[kFirst][V];
 #pragma unroll
         for (int t = 0; t < kFirst; ++t) {

@@ -152,19 +152,27 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
         constexpr int kJobs = 64 * kMaxBlock / kConsumers;  // rotation pairs per thread, at most
         // all global loads (rotation, page) first: one round trip, then the stores
         float2 cn[kJobs];
-        int page[kJobs];
+        int page[kJobs], posj[kJobs];
 #pragma unroll
         for (int u = 0; u < kJobs; ++u) {
             const int job = tid + u * kConsumers;
             cn[u] = make_float2(1.f, 0.f);
             page[u] = 0;
+            posj[u] = 0;
             if (job >= 64 * p.n) continue;
             const int j = job >> 6, pr = job & 63;
             const int hl = pr / half, i = pr - hl * half;
             const int R = (tile + p.tile0) * kTileRows + hl * hd + i;
-            const int pos = pos0 + j;
+            // batched sequences: this row's own sequence, position and page range
+            int pos = pos0 + j, pg0 = 0;
+            if (p.seq_len) {
+                const int sq = j / p.rows_per_seq;
+                pos = p.seq_len[sq] + (j - sq * p.rows_per_seq);
+                pg0 = sq * p.seq_pages;
+            }
+            posj[u] = pos;
             if (R < p.N && R < Nq + Nk) cn[u] = p.rope[(size_t)pos * half + i];
-            if (R < p.N && R >= Nq) page[u] = p.block_table[pos / kPageSize];
+            if (R < p.N && R >= Nq) page[u] = p.block_table[pg0 + pos / kPageSize];
         }
 #pragma unroll
         for (int u = 0; u < kJobs; ++u) {
@@ -177,7 +185,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             if (R >= p.N) continue;
             const float rs = sm.rstd[j];
             float va = cs[ra * kCsLd + j] * rs, vb = cs[rb * kCsLd + j] * rs;
-            const int pos = pos0 + j;
+            const int pos = posj[u];
             if (R < Nq + Nk) {
                 const float na = va * cn[u].x - vb * cn[u].y;
                 const float nb = vb * cn[u].x + va * cn[u].y;

@@ -68,6 +68,11 @@ struct GemmParams {
     // EPI_QKV
     int n_heads, n_kv_heads, head_dim;
     int tile0;                 // first 128-row tile of the full q|k|v matrix that W starts at (k/v only: q rows skipped)
+    // batched sequences (seq_len != null): row r is token r % rows_per_seq of
+    // sequence r / rows_per_seq, at position seq_len[seq] + token, whose
+    // logical pages start at seq * seq_pages of the block table
+    const int* seq_len;
+    int rows_per_seq, seq_pages;
     const float2* rope;        // [max_pos][head_dim/2] (cos, sin)
     uint16_t* qbuf;            // [16][n_heads*head_dim]
     uint16_t* kpool;           // this layer's pages [page][n_kv_heads][64][head_dim]
@@ -109,6 +114,11 @@ struct AttnParams {
     DevState* st;
     int which, n, n_heads, n_kv_heads, head_dim, nch;
     float scale_log2;          // log2(e) / sqrt(hd)
+    // batched sequences (seq_len != null): n rows per sequence, nseq of them;
+    // sequence s: positions from seq_len[s], logical pages from s * seq_pages,
+    // query rows s*n.., partials at s * n_kv_heads * nch * 64 rows
+    const int* seq_len;
+    int nseq, seq_pages;
     long long* trace;          // optional stamps of the partial kernel, then of the combine kernel
 };
 
@@ -164,7 +174,7 @@ struct RowsParams {
 };
 cudaError_t launch_rows_operand(const RowsParams& p, cudaStream_t s, bool pdl);
 
-enum AcceptMode : int { ACC_VERIFY = 0, ACC_DRAFT = 1, ACC_PREFILL = 2 };
+enum AcceptMode : int { ACC_VERIFY = 0, ACC_DRAFT = 1, ACC_PREFILL = 2, ACC_BATCH = 3 };
 struct AcceptParams {
     const float* amax_val;     // [16][T]
     const int* amax_idx;
@@ -175,6 +185,10 @@ struct AcceptParams {
     int* out_pair;             // verify: [2] or null
     int* out_token;            // draft / prefill: [1]
     DevState* st;
+    // ACC_BATCH: nseq sequences of n / nseq rows; out_accept[nseq]; each
+    // sequence keeps seq_len[s] + accept + 1 positions
+    int* seq_len;
+    int nseq;
 };
 cudaError_t launch_accept(const AcceptParams& p, cudaStream_t s, bool pdl);
 

@@ -199,6 +199,18 @@ __global__ void __launch_bounds__(512) accept_kernel(const __grid_constant__ Acc
         if (lane == 0) am[warp] = bi == 0x7fffffff ? 0 : bi;
     }
     __syncthreads();
+    if (p.mode == ACC_BATCH) {   // one thread per sequence: its rows are s*per .. s*per+per-1
+        const int per = p.n / p.nseq, sq = threadIdx.x;
+        if (sq >= p.nseq) return;
+        const int* blk = p.block + sq * per;
+        const int* a = am + sq * per;
+        int k = 0;
+        while (k < per - 1 && blk[k + 1] == a[k]) ++k;
+        for (int j = 0; j < per; ++j) p.out_argmax[sq * per + j] = a[j];
+        p.out_accept[sq] = k;
+        p.seq_len[sq] += k + 1;   // the accepted drafts and the bonus token's position are kept
+        return;
+    }
     if (threadIdx.x != 0) return;
     DevState* st = p.st;
     const int pos0 = st->len[p.which];

@@ -201,9 +201,9 @@ __device__ void attn_phase(const AttnParams& a, PassSmem& sm, int& q, bool& abor
         static_assert(attn_core::kAttnSlotBytes <= (int)sizeof(sm.g.cs), "attention scratch must fit the tile buffer");
         auto ready = [] {};   // the slab stages were waited for above
         if (a.head_dim == 128)
-            attn_core::attn_unit_c<128, 8>(a, k0, k1, v0, v1, sm.g.cs, nullptr, h, c, pos0, tid, ready);
+            attn_core::attn_unit_c<128, 8>(a, k0, k1, v0, v1, sm.g.cs, nullptr, h, c, pos0, a.n, 0, tid, ready);
         else
-            attn_core::attn_unit_c<64, 8>(a, k0, k1, v0, v1, sm.g.cs, nullptr, h, c, pos0, tid, ready);
+            attn_core::attn_unit_c<64, 8>(a, k0, k1, v0, v1, sm.g.cs, nullptr, h, c, pos0, a.n, 0, tid, ready);
         __syncwarp();
         if (lane == 0)
             for (int t = 0; t < 4; ++t) mbar_arrive(&sm.g.empty[(q + t) % kStages]);
