@@ -771,6 +771,47 @@ def suite_batch(args):
     m.close()
 
 
+def suite_shared_prefix(args):
+    """The default self-speculative cycle (Qwen3-4B, context 2048, gamma 3,
+    50% middle skip) with the draft keeping its own cache for every kept
+    layer, then with its leading layers on the target's cache (LayerSkip
+    summary 4.3.3): cycle time and the draft cache's size."""
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    cfg, w, plan, m, _ = build_model(args, torch)
+    gamma, ctx, steps = args.gamma, args.ctx, 20
+    prompt = synth.prompt(cfg, ctx)
+    shared = 0
+    while shared < len(plan) and plan[shared] == shared:
+        shared += 1
+    pages = (cfg.max_ctx + 127) // 128 * 2
+    slot_bytes = 2 * pages * cfg.n_kv_heads * 64 * cfg.head_dim * 2
+    for share in (False, True):
+        if share:
+            m.share_prefix(True)
+        load_synthetic_context(m, cfg, plan, ctx)
+        buf = torch.zeros(2 + gamma, dtype=torch.int32, device="cuda")
+        buf[0] = int(prompt[-2])
+        buf[1] = int(prompt[-1])
+        m.kv_set_len(sv.SPEC_CACHE_TARGET, ctx)
+        m.kv_set_len(sv.SPEC_CACHE_DRAFT, ctx - 1)
+        acc_log = torch.zeros(steps + 4, dtype=torch.int32, device="cuda")
+        device_cycles(m, torch, gamma, 3, buf, acc_log, 0)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        device_cycles(m, torch, gamma, steps, buf, acc_log, 3)
+        e1.record()
+        torch.cuda.synchronize()
+        own = len(plan) - (shared if share else 0)
+        _emit({"suite": "shared_prefix", "config": args.config, "ctx": ctx, "gamma": gamma, "skip_frac": args.skip,
+               "shared_prefix": share, "shared_layers": shared, "draft_cache_slots": own,
+               "draft_cache_bytes": own * slot_bytes, "cycle_ms": round(e0.elapsed_time(e1) / steps, 4)})
+    m.check_error()
+    m.close()
+
+
 def suite_moe(args):
     """DeepSeek-V2-Lite-shaped MoE verify at n = 1..8 with forced synthetic
     routing traces: per-slot vs deduplicated expert reads (time, requested
@@ -915,14 +956,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for counter captures; the line names it)")
-    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "batch", "moe", "extras"],
+    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "batch", "shared_prefix", "moe", "extras"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
     if args.suite:
         import __graft_entry__
         __graft_entry__.build()
         {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash,
-         "dflash_block": suite_dflash_block, "batch": suite_batch, "moe": suite_moe,
+         "dflash_block": suite_dflash_block, "batch": suite_batch, "shared_prefix": suite_shared_prefix,
+         "moe": suite_moe,
          "extras": suite_extras}[args.suite](args)
         return
     if args.warmup < 3:

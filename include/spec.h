@@ -186,6 +186,18 @@ spec_status spec_kv_rollback(spec_handle h, int32_t which, int32_t new_len);
  * bitwise identical outputs. */
 spec_status spec_moe_mode(spec_handle h, int32_t mode);
 
+/* Shared prefix cache (next row NEXT-1; LayerSkip summary 4.3.3, "Single KV
+ * Cache").  The draft plan's leading layers 0..E-1 (E = the length of its
+ * contiguous prefix 0, 1, 2, ...) compute exactly what the target computes
+ * for the same tokens, so with enable != 0 the draft uses the target's KV
+ * cache for them and keeps its own cache only for its other layers (E fewer
+ * slots are allocated).  Values the draft writes ahead of the target are the
+ * ones the target's verify writes again (the passes are batch-invariant).
+ * Reallocates the draft cache and sets its length to 0 (prefill again);
+ * drops captured launch sequences; synchronises the stream.  SPEC_ERR_STATE
+ * without a draft plan.  A later spec_set_draft_plan keeps the setting. */
+spec_status spec_share_prefix(spec_handle h, int32_t enable);
+
 /* Hidden-state taps (mlx-dflash README, "Architecture": the draft's context
  * features are taken from the target's hidden states at chosen layers).
  * After this call every target verify pass also writes, for each of its n

@@ -29,7 +29,7 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds",
             "spec_set_taps", "spec_set_context_fc", "spec_context_append", "spec_batch_reserve",
             "spec_batch_kv_load", "spec_batch_kv_export", "spec_batch_set_len", "spec_batch_len",
-            "spec_verify_batch"]
+            "spec_verify_batch", "spec_share_prefix"]
 
 
 class SpecError(RuntimeError):
@@ -86,6 +86,7 @@ def library():
         "spec_set_taps": [vp, vp, i32, vp],
         "spec_set_context_fc": [vp, vp, i32],
         "spec_batch_reserve": [vp, i32],
+        "spec_share_prefix": [vp, i32],
         "spec_batch_kv_load": [vp, i32, i32, vp, vp, i32],
         "spec_batch_kv_export": [vp, i32, i32, vp, vp, i32],
         "spec_batch_set_len": [vp, i32, i32],
@@ -169,6 +170,10 @@ def spec_set_context_fc(h, d_fc, n_in: int):
 
 def spec_context_append(h, d_taps, m: int):
     _check(library().spec_context_append(h, _ptr(d_taps), int(m)))
+
+
+def spec_share_prefix(h, enable: bool):
+    _check(library().spec_share_prefix(h, 1 if enable else 0))
 
 
 def spec_batch_reserve(h, nseq: int):
@@ -399,6 +404,11 @@ class Model:
         """Append m context positions from tapped hidden states (a device
         fp32 tensor [n_in][16][d_model], e.g. a target's set_taps buffer)."""
         spec_context_append(self.h, taps, m)
+
+    def share_prefix(self, enable=True):
+        """The draft's leading layers use the target's KV cache (the draft
+        cache is reallocated and emptied)."""
+        spec_share_prefix(self.h, enable)
 
     def batch_reserve(self, nseq):
         spec_batch_reserve(self.h, nseq)

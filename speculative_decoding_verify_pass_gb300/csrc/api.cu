@@ -142,6 +142,8 @@ struct spec_model {
     std::vector<ProfRec> prof;
     std::vector<void*> allocs;
     std::vector<void*> draft_allocs;
+    bool share_prefix = false;          // the draft's leading layers 0..n_shared-1 use the target's caches
+    int n_shared = 0;                   // layers the draft plan shares with the target as a contiguous prefix
 };
 
 namespace {
@@ -242,15 +244,29 @@ spec_status validate_plan(const spec_model* h, const int32_t* layers, int32_t n)
     return SPEC_OK;
 }
 
+// The K (kv = 0) or V (kv = 1) pool of cache `which`, slot `si` (plan index;
+// the layer itself for the target).  With a shared prefix the draft's first
+// n_shared slots are the target's pools of the same layers (LayerSkip
+// summary 4.3.3: one KV cache for the layers both stages run identically).
+uint16_t* kv_pool(spec_model* h, int which, int si, int kv) {
+    if (which == 0) return (kv ? h->vt : h->kt) + h->pool_elems * si;
+    if (h->share_prefix && si < h->n_shared) return (kv ? h->vt : h->kt) + h->pool_elems * si;
+    const int own = h->share_prefix ? si - h->n_shared : si;
+    return (kv ? h->vd : h->kd) + h->pool_elems * own;
+}
+
 spec_status alloc_draft(spec_model* h, const int32_t* layers, int32_t n) {
     for (void* p : h->draft_allocs) cudaFree(p);
     h->draft_allocs.clear();
     h->kd = h->vd = nullptr;
     h->plan_draft.assign(layers, layers + n);
-    if (n > 0) {
+    h->n_shared = 0;
+    while (h->n_shared < n && layers[h->n_shared] == h->n_shared) ++h->n_shared;
+    const int own = h->share_prefix ? n - h->n_shared : n;   // slots the draft keeps for itself
+    if (own > 0) {
         spec_status s;
-        if ((s = dalloc_t(h, &h->kd, h->pool_elems * n, &h->draft_allocs)) != SPEC_OK) return s;
-        if ((s = dalloc_t(h, &h->vd, h->pool_elems * n, &h->draft_allocs)) != SPEC_OK) return s;
+        if ((s = dalloc_t(h, &h->kd, h->pool_elems * own, &h->draft_allocs)) != SPEC_OK) return s;
+        if ((s = dalloc_t(h, &h->vd, h->pool_elems * own, &h->draft_allocs)) != SPEC_OK) return s;
     }
     h->host_len[1] = 0;
     h->len_exact[1] = true;
@@ -480,8 +496,8 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         float* tap = (which == 0 && mode == PASS_VERIFY && h->tap_count > 0 && h->tap_of_layer[l] >= 0)
                          ? h->tap_out + (size_t)h->tap_of_layer[l] * kMaxBlock * d
                          : nullptr;
-        uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
-        uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
+        uint16_t* kpool = kv_pool(h, which, which == 0 ? l : (int)si, 0);
+        uint16_t* vpool = kv_pool(h, which, which == 0 ? l : (int)si, 1);
         const bool bat = h->bat_nseq > 0;   // batched sequences: their own caches, positions and pages
         const int rps = bat ? n / h->bat_nseq : n;
         if (bat) {
@@ -702,8 +718,8 @@ spec_status pass_table(spec_model* h, int which, int n, bool lm, spec_model::Pas
         const int l = plan[si];
         LayerW& W = h->L[l];
         const uint16_t* g_after = (si + 1 < plan.size()) ? h->L[plan[si + 1]].attn_norm : h->final_norm;
-        uint16_t* kpool = (which == 0 ? h->kt + h->pool_elems * l : h->kd + h->pool_elems * si);
-        uint16_t* vpool = (which == 0 ? h->vt + h->pool_elems * l : h->vd + h->pool_elems * si);
+        uint16_t* kpool = kv_pool(h, which, which == 0 ? l : (int)si, 0);
+        uint16_t* vpool = kv_pool(h, which, which == 0 ? l : (int)si, 1);
         GemmParams p = base_params(h, which, n);
         set_mat(h, p, W.qkv, h->xf_norm, EPI_QKV, G);
         p.norm_dim = d;
@@ -1155,6 +1171,26 @@ spec_status spec_moe_mode(spec_handle h, int32_t mode) {
     return SPEC_OK;
 }
 
+spec_status spec_share_prefix(spec_handle h, int32_t enable) {
+    if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
+    if (h->plan_draft.empty()) return fail(SPEC_ERR_STATE, "model has no draft plan");
+    CU(cudaStreamSynchronize(h->stream));
+    clear_graphs(h);
+    for (auto it = h->tables.begin(); it != h->tables.end();) {
+        if (it->first / 10000 == 1)
+            it = h->tables.erase(it);   // draft tables point at the old draft pools
+        else
+            ++it;
+    }
+    h->share_prefix = enable != 0;
+    const std::vector<int32_t> plan = h->plan_draft;
+    spec_status s = alloc_draft(h, plan.data(), (int32_t)plan.size());
+    if (s != SPEC_OK) return s;
+    CU(launch_rollback(h->st, 1, 0, h->stream, false));
+    CU(cudaStreamSynchronize(h->stream));
+    return SPEC_OK;
+}
+
 spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, float* d_out) {
     if (!h) return fail(SPEC_ERR_INVALID_ARG, "null handle");
     if (count < 0 || count > h->c.n_layers) return fail(SPEC_ERR_INVALID_ARG, "tap count %d out of range", count);
@@ -1368,8 +1404,8 @@ static spec_status kv_io(spec_handle h, int32_t which, int32_t slot, void* dk, v
     const int nslots = which == 0 ? h->c.n_layers : (int)h->plan_draft.size();
     if (slot < 0 || slot >= nslots) return fail(SPEC_ERR_INVALID_ARG, "slot %d out of range", slot);
     if (ctx < 0 || ctx > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "ctx %d out of range", ctx);
-    uint16_t* kp = (which == 0 ? h->kt : h->kd) + h->pool_elems * slot;
-    uint16_t* vp = (which == 0 ? h->vt : h->vd) + h->pool_elems * slot;
+    uint16_t* kp = kv_pool(h, which, slot, 0);
+    uint16_t* vp = kv_pool(h, which, slot, 1);
     CU(launch_kv_io(kp, h->block_table, static_cast<uint16_t*>(dk), ctx, h->c.n_kv_heads, h->c.head_dim, load, h->stream));
     CU(launch_kv_io(vp, h->block_table, static_cast<uint16_t*>(dv), ctx, h->c.n_kv_heads, h->c.head_dim, load, h->stream));
     return SPEC_OK;
