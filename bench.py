@@ -885,6 +885,215 @@ def suite_moe(args):
     m.close()
 
 
+def suite_selfspec(args):
+    """The MLX self-speculation post's grid on the Qwen3-4B shape at context
+    2048 (seeded synthetic KV): for every middle-skip fraction 10..50% and
+    draft length 2, 3, 5, device-resident self-speculative cycles against
+    plain greedy decoding (one verify of one token per token), timed back to
+    back; reports the measured acceptance on the random-init model, the
+    verify pass at n = gamma+1 and the draft step."""
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    ctx = args.ctx
+    cfg = synth.qwen3_4b(max_ctx=ctx + 1024)
+    w = synth.make_weights(cfg)
+    m = sv.Model(cfg, w, draft_plan=sv.layer_skip_plan(cfg.n_layers, 0.5))
+    kv = [(synth.synthetic_kv(cfg, l, ctx, 0), synth.synthetic_kv(cfg, l, ctx, 1)) for l in range(cfg.n_layers)]
+    for l in range(cfg.n_layers):
+        m.kv_load(0, l, *kv[l])
+    prompt = synth.prompt(cfg, ctx)
+    steps = max(args.steps, 8)
+
+    def timed(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3   # s
+
+    # plain greedy: verify n=1 per token; the verify's catch-up pair carries the next input
+    pbuf = torch.tensor([int(prompt[-2]), int(prompt[-1])], dtype=torch.int32, device="cuda")
+    am1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ac1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+    def plain(k):
+        for _ in range(k):
+            sv.spec_verify_step(m.h, pbuf[1:2], am1, ac1, None, None, pbuf[0:2])
+            sv.spec_kv_rollback(m.h, sv.SPEC_CACHE_TARGET, -1)
+
+    def plain_rate():
+        m.kv_set_len(sv.SPEC_CACHE_TARGET, ctx)
+        plain(3)
+        s = timed(lambda: plain(steps))
+        m.check_error()
+        return steps / s
+
+    for f in (0.1, 0.2, 0.3, 0.4, 0.5):
+        plan = sv.layer_skip_plan(cfg.n_layers, f)
+        m.set_draft_plan(plan)
+        for i, l in enumerate(plan):
+            m.kv_load(1, i, *kv[l])
+        m.kv_set_len(sv.SPEC_CACHE_DRAFT, ctx)
+        t_draft = _draft_us(torch, sv, m, ctx)
+        for gamma in (2, 3, 5):
+            n = gamma + 1
+            m.kv_set_len(sv.SPEC_CACHE_TARGET, ctx)
+            t_verify = _verify_us(torch, sv, m, prompt[:n].tolist(), ctx)
+            buf = torch.zeros(2 + gamma, dtype=torch.int32, device="cuda")
+            buf[0] = int(prompt[-2])
+            buf[1] = int(prompt[-1])
+            m.kv_set_len(sv.SPEC_CACHE_TARGET, ctx)
+            m.kv_set_len(sv.SPEC_CACHE_DRAFT, ctx - 1)
+            acc_log = torch.zeros(steps + 3, dtype=torch.int32, device="cuda")
+            device_cycles(m, torch, gamma, 3, buf, acc_log, 0)
+            s = timed(lambda: device_cycles(m, torch, gamma, steps, buf, acc_log, 3))
+            m.check_error()
+            acc = acc_log[3:].cpu().numpy()
+            tokens = float(np.sum(acc + 1))
+            spec = tokens / s
+            base = plain_rate()
+            _emit({"suite": "selfspec", "config": cfg.name, "ctx": ctx, "skip_frac": f, "draft_layers": len(plan),
+                   "gamma": gamma, "cycles": steps, "accept_mean": round(float(np.mean(acc)), 3),
+                   "accept_rate": round(float(np.mean(acc)) / gamma, 4), "tokens_per_cycle": round(tokens / steps, 3),
+                   "selfspec_tok_s": round(spec, 1), "plain_tok_s": round(base, 1),
+                   "speedup": round(spec / base, 3), "verify_us": round(t_verify, 1), "draft_us": round(t_draft, 1)})
+    m.close()
+
+
+def suite_moe_bytes(args):
+    """Expert bytes of one MoE verify pass (n = 8, forced synthetic routing)
+    in both modes, for a counter capture: the DeepSeek-V2-Lite shape cut to
+    its dense layer 0 and two MoE layers and a 16384-token vocabulary (the
+    expert shapes are the full model's; a small device footprint keeps the
+    counters' memory save and restore short), context 2048.  Prints per mode the
+    analytic bytes each expert launch requests (per slot: one expert read per
+    token and slot; dedup: one per distinct expert) and the launch order, so
+    that DRAM and L2 counters of the same launches can be set beside them.
+    Each mode's pass runs inside an NVTX range "timed"."""
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+    ctx, n = 2048, 8
+    cfg = synth.scaled(synth.moe_v2lite(max_ctx=ctx + 64), n_layers=3, vocab=16384)
+    m, _ = _model_at_context(cfg, ctx)
+    trace = synth.routing_trace(cfg.n_layers, 16, cfg.n_experts, cfg.top_k)
+    m.force_routing(trace)
+    toks = synth.prompt(cfg, n).tolist()
+    blk = torch.tensor(toks, dtype=torch.int32, device="cuda")
+    am = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gate_up = 2 * cfg.expert_ffn * cfg.d_model * 2
+    down = cfg.expert_ffn * cfg.d_model * 2
+    for mode, name in ((sv.SPEC_MOE_PER_SLOT, "per_slot"), (sv.SPEC_MOE_DEDUP, "dedup")):
+        m.moe_mode(mode)
+        for _ in range(3):
+            sv.spec_verify_step(m.h, blk, am, ac)
+            sv.spec_kv_rollback(m.h, 0, ctx)
+        torch.cuda.synchronize()
+        torch.cuda.nvtx.range_push("timed")
+        sv.spec_verify_step(m.h, blk, am, ac)
+        torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        launches = m.launches()
+        sv.spec_kv_rollback(m.h, 0, ctx)
+        m.check_error()
+        layers = []
+        for l in range(cfg.first_moe_layer, cfg.n_layers):
+            u = stepmodel.union_size(trace[l, :n])
+            reads = n * cfg.top_k if name == "per_slot" else u
+            layers.append({"layer": l, "unique_experts": u, "expert_reads": reads,
+                           "gate_up_bytes": reads * gate_up, "down_bytes": reads * down,
+                           "unique_gate_up_bytes": u * gate_up, "unique_down_bytes": u * down})
+        _emit({"suite": "moe_bytes", "config": cfg.name + ", first 3 layers, vocab 16384", "ctx": ctx, "n": n, "mode": name,
+               "launches": launches, "layers": layers})
+    m.close()
+
+
+TRACE_KIND_NAMES = {0: "qkv", 1: "resid", 2: "swiglu", 3: "lm_head", 4: "router", 5: "expert_gate_up",
+                    6: "expert_down", 7: "store", 16: "attn_partial", 17: "attn_merge", 18: "embed", 19: "accept"}
+
+
+def trace_breakdown(stamps, kinds):
+    """Per launch kind, from the per-CTA global-timer stamps of one traced
+    pass ([ctas][launches][entry, inputs ready, main work done, exit]): mean
+    microseconds from the launch's inputs being ready (earliest CTA) to its
+    last CTA's exit, from its last main-work stamp to that exit, and from
+    the previous launch's last exit to this launch's inputs being ready;
+    plus the pass's span from the first entry to the last exit."""
+    out, prev_exit = {}, None
+    first, last = None, None
+    for l, kind in enumerate(kinds):
+        s = stamps[:, l, :]
+        live = s[s[:, 0] > 0]
+        if len(live) == 0:
+            continue
+        rd = live[live[:, 1] > 0, 1]
+        ready = int(rd.min()) if len(rd) else int(live[:, 0].min())
+        wk = live[live[:, 2] > 0, 2]
+        ex = int(live[:, 3].max())
+        e = out.setdefault(TRACE_KIND_NAMES.get(int(kind), str(int(kind))),
+                           {"launches": 0, "ready_to_exit": 0.0, "work_to_exit": 0.0, "gap": 0.0, "gaps": 0})
+        e["launches"] += 1
+        e["ready_to_exit"] += (ex - ready) / 1e3
+        if len(wk):
+            e["work_to_exit"] += (ex - int(wk.max())) / 1e3
+        if prev_exit is not None:
+            e["gap"] += (ready - prev_exit) / 1e3
+            e["gaps"] += 1
+        prev_exit = ex
+        first = int(live[:, 0].min()) if first is None else min(first, int(live[:, 0].min()))
+        last = ex if last is None else max(last, ex)
+    for e in out.values():
+        k = e["launches"]
+        e["ready_to_exit"] = round(e["ready_to_exit"] / k, 2)
+        e["work_to_exit"] = round(e["work_to_exit"] / k, 2)
+        e["gap"] = round(e["gap"] / max(e.pop("gaps"), 1), 2)
+    return out, (last - first) / 1e3 if first is not None else 0.0
+
+
+def suite_trace(args):
+    """Where a verify pass's time goes: the launch trace (per-CTA global-timer
+    stamps, separate launches) of the Qwen3-4B-shaped verify at context 2048
+    for n = 1, 4, 8, 16, summarised per launch kind."""
+    import torch
+    import synth
+    import speculative_decoding_verify_pass_gb300 as sv
+    ctx = args.ctx
+    cfg = synth.qwen3_4b(max_ctx=ctx + 64)
+    m, _ = _model_at_context(cfg, ctx)
+    for n in (1, 4, 8, 16):
+        toks = synth.prompt(cfg, n).tolist()
+        blk = torch.tensor(toks, dtype=torch.int32, device="cuda")
+        am = torch.zeros(n, dtype=torch.int32, device="cuda")
+        ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sv.spec_trace_enable(m.h, True)
+        spans, acc = [], {}
+        for r in range(4):
+            sv.spec_verify_step(m.h, blk, am, ac)
+            sv.spec_kv_rollback(m.h, 0, ctx)
+            torch.cuda.synchronize()
+            if r == 0:
+                continue   # first traced pass warms the direct-launch path
+            per, span = trace_breakdown(sv.spec_trace_read(m.h), sv.spec_trace_kinds(m.h))
+            spans.append(span)
+            for k, e in per.items():
+                a = acc.setdefault(k, {"launches": e["launches"], "ready_to_exit": 0.0, "work_to_exit": 0.0, "gap": 0.0})
+                for f in ("ready_to_exit", "work_to_exit", "gap"):
+                    a[f] += e[f] / 3
+        sv.spec_trace_enable(m.h, False)
+        m.check_error()
+        for a in acc.values():
+            for f in ("ready_to_exit", "work_to_exit", "gap"):
+                a[f] = round(a[f], 2)
+        _emit({"suite": "trace", "config": cfg.name, "ctx": ctx, "n": n, "traced_pass_us": round(float(np.mean(spans)), 1),
+               "verify_us_graph": round(_verify_us(torch, sv, m, toks, ctx), 1), "per_kind_us": acc})
+    m.close()
+
+
 def suite_extras(args):
     """The tiny config (correctness-size model: greedy vs self-speculative
     tokens/s at gamma 4 over the middle-two-of-four plan, verify time per
@@ -956,7 +1165,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for counter captures; the line names it)")
-    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "batch", "shared_prefix", "moe", "extras"],
+    ap.add_argument("--suite", default=None, choices=["sweep", "geometric", "dflash", "dflash_block", "batch", "shared_prefix", "moe", "moe_bytes",
+                             "selfspec", "trace", "extras"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
     if args.suite:
@@ -964,7 +1174,8 @@ def main():
         __graft_entry__.build()
         {"sweep": suite_sweep, "geometric": suite_geometric, "dflash": suite_dflash,
          "dflash_block": suite_dflash_block, "batch": suite_batch, "shared_prefix": suite_shared_prefix,
-         "moe": suite_moe,
+         "moe": suite_moe, "moe_bytes": suite_moe_bytes, "selfspec": suite_selfspec,
+         "trace": suite_trace,
          "extras": suite_extras}[args.suite](args)
         return
     if args.warmup < 3:
