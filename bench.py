@@ -1017,12 +1017,18 @@ TRACE_KIND_NAMES = {0: "qkv", 1: "resid", 2: "swiglu", 3: "lm_head", 4: "router"
                     6: "expert_down", 7: "store", 16: "attn_partial", 17: "attn_merge", 18: "embed", 19: "accept"}
 
 
+TRACE_FIELDS = ("ready_to_exit", "work_to_exit", "gap", "ready_spread", "cta_ready_to_work_med",
+                "cta_ready_to_work_max", "work_spread")
+
+
 def trace_breakdown(stamps, kinds):
     """Per launch kind, from the per-CTA global-timer stamps of one traced
     pass ([ctas][launches][entry, inputs ready, main work done, exit]): mean
     microseconds from the launch's inputs being ready (earliest CTA) to its
     last CTA's exit, from its last main-work stamp to that exit, and from
     the previous launch's last exit to this launch's inputs being ready;
+    the spread of the CTAs' ready stamps, the median and largest per-CTA time
+    from ready to main work done, and the spread of the main-work stamps;
     plus the pass's span from the first entry to the last exit."""
     out, prev_exit = {}, None
     first, last = None, None
@@ -1036,11 +1042,21 @@ def trace_breakdown(stamps, kinds):
         wk = live[live[:, 2] > 0, 2]
         ex = int(live[:, 3].max())
         e = out.setdefault(TRACE_KIND_NAMES.get(int(kind), str(int(kind))),
-                           {"launches": 0, "ready_to_exit": 0.0, "work_to_exit": 0.0, "gap": 0.0, "gaps": 0})
+                           {"launches": 0, "ready_to_exit": 0.0, "work_to_exit": 0.0, "gap": 0.0, "gaps": 0,
+                            "ready_spread": 0.0, "cta_ready_to_work_med": 0.0, "cta_ready_to_work_max": 0.0,
+                            "work_spread": 0.0})
         e["launches"] += 1
         e["ready_to_exit"] += (ex - ready) / 1e3
+        if len(rd):
+            e["ready_spread"] += (int(rd.max()) - ready) / 1e3
         if len(wk):
             e["work_to_exit"] += (ex - int(wk.max())) / 1e3
+            e["work_spread"] += (int(wk.max()) - int(wk.min())) / 1e3
+            both = live[(live[:, 1] > 0) & (live[:, 2] > 0)]
+            if len(both):
+                w = (both[:, 2] - both[:, 1]) / 1e3
+                e["cta_ready_to_work_med"] += float(np.median(w))
+                e["cta_ready_to_work_max"] += float(w.max())
         if prev_exit is not None:
             e["gap"] += (ready - prev_exit) / 1e3
             e["gaps"] += 1
@@ -1049,8 +1065,9 @@ def trace_breakdown(stamps, kinds):
         last = ex if last is None else max(last, ex)
     for e in out.values():
         k = e["launches"]
-        e["ready_to_exit"] = round(e["ready_to_exit"] / k, 2)
-        e["work_to_exit"] = round(e["work_to_exit"] / k, 2)
+        for f in ("ready_to_exit", "work_to_exit", "ready_spread", "cta_ready_to_work_med", "cta_ready_to_work_max",
+                  "work_spread"):
+            e[f] = round(e[f] / k, 2)
         e["gap"] = round(e["gap"] / max(e.pop("gaps"), 1), 2)
     return out, (last - first) / 1e3 if first is not None else 0.0
 
@@ -1081,13 +1098,14 @@ def suite_trace(args):
             per, span = trace_breakdown(sv.spec_trace_read(m.h), sv.spec_trace_kinds(m.h))
             spans.append(span)
             for k, e in per.items():
-                a = acc.setdefault(k, {"launches": e["launches"], "ready_to_exit": 0.0, "work_to_exit": 0.0, "gap": 0.0})
-                for f in ("ready_to_exit", "work_to_exit", "gap"):
+                a = acc.setdefault(k, {f: 0.0 for f in TRACE_FIELDS})
+                a["launches"] = e["launches"]
+                for f in TRACE_FIELDS:
                     a[f] += e[f] / 3
         sv.spec_trace_enable(m.h, False)
         m.check_error()
         for a in acc.values():
-            for f in ("ready_to_exit", "work_to_exit", "gap"):
+            for f in TRACE_FIELDS:
                 a[f] = round(a[f], 2)
         _emit({"suite": "trace", "config": cfg.name, "ctx": ctx, "n": n, "traced_pass_us": round(float(np.mean(spans)), 1),
                "verify_us_graph": round(_verify_us(torch, sv, m, toks, ctx), 1), "per_kind_us": acc})

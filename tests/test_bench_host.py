@@ -30,8 +30,14 @@ def test_trace_breakdown_per_kind():
     ])
     out, span = bench.trace_breakdown(st, [0, 16, 0])
     assert span == 12.0
-    assert out["qkv"] == {"launches": 2, "ready_to_exit": 4.0, "work_to_exit": 1.25, "gap": 1.0}
-    assert out["attn_partial"] == {"launches": 1, "ready_to_exit": 1.0, "work_to_exit": 0.0, "gap": 1.0}
+    q = out["qkv"]
+    assert (q["launches"], q["ready_to_exit"], q["work_to_exit"], q["gap"]) == (2, 4.0, 1.25, 1.0)
+    assert q["ready_spread"] == 0.05            # (100 + 0) / 2 launches
+    assert q["cta_ready_to_work_med"] == 2.6    # medians 3.2 and 2.0
+    assert q["cta_ready_to_work_max"] == 2.7    # maxima 3.4 and 2.0
+    assert q["work_spread"] == 0.25             # (500 + 0) / 2
+    a = out["attn_partial"]
+    assert (a["launches"], a["ready_to_exit"], a["work_to_exit"], a["gap"]) == (1, 1.0, 0.0, 1.0)
 
 
 def test_trace_breakdown_skips_launches_without_live_ctas_and_uses_entry_when_never_waited():
