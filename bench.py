@@ -830,6 +830,8 @@ def suite_moe(args):
     trace = synth.routing_trace(L, 16, cfg.n_experts, cfg.top_k)       # [layer][token][k]
     m.force_routing(trace)
     per_expert = stepmodel.expert_bytes(cfg)
+    # the shared experts are work items of the same launches, read once per pass in both modes
+    shared_bytes = (L - cfg.first_moe_layer) * cfg.n_shared_experts * per_expert
     rows = {}
     for n in range(1, 9):
         toks = synth.prompt(cfg, n).tolist()
@@ -853,7 +855,8 @@ def suite_moe(args):
             rows[(n, name)] = (us, exp_us, exp_bytes)
             _emit({"suite": "moe", "config": "moe-v2-lite", "ctx": ctx, "n": n, "mode": name,
                    "verify_us": round(us, 1), "expert_us": round(exp_us, 1),
-                   "expert_bytes_requested": int(exp_bytes), "expert_GBps": round(exp_bytes / exp_us / 1e3, 1),
+                   "expert_bytes_requested": int(exp_bytes), "routed_bytes_requested": int(exp_bytes - shared_bytes),
+                   "expert_GBps": round(exp_bytes / exp_us / 1e3, 1),
                    "unique_experts_mean": round(float(np.mean(u_layers)), 2),
                    "unique_experts_expected": round(stepmodel.union_size_expected(n, cfg.n_experts, cfg.top_k), 2)})
     # crossover: measured (verify time) and predicted (bytes over bandwidths fitted at one pass size)
@@ -972,6 +975,8 @@ def suite_moe_bytes(args):
     analytic bytes each expert launch requests (per slot: one expert read per
     token and slot; dedup: one per distinct expert) and the launch order, so
     that DRAM and L2 counters of the same launches can be set beside them.
+    The shared experts are items of the same launches and are counted in
+    both the reads and the unique experts.
     Each mode's pass runs inside an NVTX range "timed"."""
     import torch
     import synth
@@ -1004,7 +1009,8 @@ def suite_moe_bytes(args):
         layers = []
         for l in range(cfg.first_moe_layer, cfg.n_layers):
             u = stepmodel.union_size(trace[l, :n])
-            reads = n * cfg.top_k if name == "per_slot" else u
+            reads = (n * cfg.top_k if name == "per_slot" else u) + cfg.n_shared_experts   # + shared, once each
+            u += cfg.n_shared_experts
             layers.append({"layer": l, "unique_experts": u, "expert_reads": reads,
                            "gate_up_bytes": reads * gate_up, "down_bytes": reads * down,
                            "unique_gate_up_bytes": u * gate_up, "unique_down_bytes": u * down})

@@ -49,8 +49,8 @@ enum PassMode { PASS_VERIFY, PASS_DRAFT, PASS_PREFILL_LAST, PASS_PREFILL_MID };
 struct LayerW {
     bool moe = false;
     PackedMat qkv, o, gu, down;         // dense FFN in gu/down
-    PackedMat router, sgu, sdown;       // MoE
-    PackedMat egu, edown;               // geometry of one expert; experts at a fixed stride
+    PackedMat router;                   // MoE
+    PackedMat egu, edown;               // geometry of one expert; routed experts then shared ones, at a fixed stride
     long long egu_stride = 0, edown_stride = 0;
     uint16_t* attn_norm = nullptr;
     uint16_t* ffn_norm = nullptr;
@@ -74,7 +74,7 @@ struct spec_model {
     uint16_t *kt = nullptr, *vt = nullptr, *kd = nullptr, *vd = nullptr;
     std::vector<int> plan_full, plan_draft;
     float* x = nullptr;
-    uint8_t *xf_norm = nullptr, *xf_o = nullptr, *xf_down = nullptr, *xs = nullptr, *xe = nullptr;
+    uint8_t *xf_norm = nullptr, *xf_o = nullptr, *xf_down = nullptr, *xe = nullptr;
     long long xe_stride = 0;
     uint16_t* qbuf = nullptr;
     float* ss = nullptr;
@@ -105,7 +105,6 @@ struct spec_model {
     float* tap_out = nullptr;           // caller's [count][16][d_model] fp32 buffer
     int tap_count = 0;
     float* y_slot = nullptr;
-    float* ys = nullptr;
     DevState* st = nullptr;
     int moe_mode = SPEC_MOE_DEDUP;
     int host_len[2] = {0, 0};   // upper bounds of the device lengths
@@ -314,6 +313,7 @@ GemmParams base_params(spec_model* h, int which, int n) {
     p.head_dim = h->c.head_dim;
     p.n_experts = h->c.n_experts;
     p.top_k = h->c.top_k;
+    p.n_shared = h->c.n_experts > 0 ? h->c.n_shared_experts : 0;
     p.moe_mode = h->moe_mode;
     return p;
 }
@@ -352,7 +352,8 @@ double gemm_bytes(const GemmParams& p) {
 
 // Expert weight bytes one items-mode launch requests: per-slot reads one
 // expert per (token, slot), dedup one per distinct expert (needs the ids on
-// the host, i.e. forced routing; otherwise the per-slot count is reported).
+// the host, i.e. forced routing; otherwise the per-slot count is reported);
+// both read every shared expert once.
 double expert_launch_bytes(spec_model* h, const GemmParams& p, int layer) {
     const double per = (double)p.N * p.KBs * kKBlock * 2.0;
     const int K = h->c.top_k, n = p.n;
@@ -363,6 +364,7 @@ double expert_launch_bytes(spec_model* h, const GemmParams& p, int layer) {
             for (int s = 0; s < K; ++s) used |= 1ull << (h->forced_host[((size_t)layer * kMaxBlock + j) * K + s] & 63);
         items = __builtin_popcountll(used);
     }
+    items += h->c.n_shared_experts;   // shared experts: once per launch in both modes
     return items * per + (double)n * p.KBs * kKBlock * 2.0;
 }
 
@@ -576,15 +578,8 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             p.forced_ids = h->forced_on ? h->forced + (size_t)l * kMaxBlock * K : nullptr;
             p.debug_ids = (d_ids && which == 0) ? d_ids + (size_t)l * n * K : nullptr;
             if ((s = gemm(h, p)) != SPEC_OK) return s;
-            // shared experts (dense SwiGLU over all tokens)
-            if (c.n_shared_experts > 0) {
-                p = base_params(h, which, n);
-                set_mat(h, p, W.sgu, h->xf_norm, EPI_SWIGLU, G);
-                p.norm_dim = d;
-                p.xf_out = h->xs;
-                if ((s = gemm(h, p)) != SPEC_OK) return s;
-            }
-            // routed experts, gate/up: per-slot or deduplicated work items
+            // routed experts, gate/up: per-slot or deduplicated work items; the
+            // shared experts are further items of the same launches
             p = base_params(h, which, n);
             set_mat(h, p, W.egu, h->xf_norm, EPI_EXPERT_SWIGLU, G);
             p.items_mode = 1;
@@ -596,12 +591,6 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             p.xe = h->xe;
             p.xe_stride = h->xe_stride;
             if ((s = gemm(h, p, l)) != SPEC_OK) return s;
-            if (c.n_shared_experts > 0) {
-                p = base_params(h, which, n);
-                set_mat(h, p, W.sdown, h->xs, EPI_STORE, G);
-                p.y_store = h->ys;
-                if ((s = gemm(h, p)) != SPEC_OK) return s;
-            }
             p = base_params(h, which, n);
             set_mat(h, p, W.edown, h->xe, EPI_EXPERT_DOWN, G);
             p.items_mode = 1;
@@ -614,7 +603,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
             CombineParams cb{};
             cb.x = h->x;
             cb.y_slot = h->y_slot;
-            cb.y_shared = c.n_shared_experts > 0 ? h->ys : nullptr;
+            cb.n_shared = c.n_shared_experts;
             cb.gates = h->route_gates;
             cb.n = n;
             cb.d = d;
@@ -952,39 +941,19 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
             W.edown_stride = (long long)d1.bytes();
             W.egu = g1;
             W.edown = d1;
-            TRY(dalloc(h, reinterpret_cast<void**>(&W.egu.p), g1.bytes() * c.n_experts));
-            TRY(dalloc(h, reinterpret_cast<void**>(&W.edown.p), d1.bytes() * c.n_experts));
+            TRY(dalloc(h, reinterpret_cast<void**>(&W.egu.p), g1.bytes() * (c.n_experts + S)));
+            TRY(dalloc(h, reinterpret_cast<void**>(&W.edown.p), d1.bytes() * (c.n_experts + S)));
             if (g1.T > h->max_T) h->max_T = g1.T;
             if (d1.T > h->max_T) h->max_T = d1.T;
-            for (int e = 0; e < c.n_experts; ++e) {
+            for (int e = 0; e < c.n_experts + S; ++e) {   // shared expert t at index n_experts + t
                 PackedMat ge = g1, de = d1;
                 ge.p = W.egu.p + e * W.egu_stride;
                 de.p = W.edown.p + e * W.edown_stride;
-                TRY(pack_into(h, ge, src_rows({lw.e_gate[e], lw.e_up[e]}, {fe, fe}, d, 1)));
-                TRY(pack_into(h, de, src_rows({lw.e_down[e]}, {d}, fe, 0)));
-            }
-            if (S > 0) {
-                TRY(alloc_packed(h, W.sgu, 2 * S * fe, d));
-                PackSrc ps{};
-                for (int e = 0; e < S; ++e) {
-                    ps.src[e] = static_cast<const uint16_t*>(lw.s_gate[e]);
-                    ps.src[S + e] = static_cast<const uint16_t*>(lw.s_up[e]);
-                    ps.rows[e] = ps.rows[S + e] = fe;
-                }
-                ps.nsrc = 2 * S;
-                ps.cols = d;
-                ps.mode = 1;
-                TRY(pack_into(h, W.sgu, ps));
-                TRY(alloc_packed(h, W.sdown, d, S * fe));
-                PackSrc pd{};
-                for (int e = 0; e < S; ++e) {
-                    pd.src[e] = static_cast<const uint16_t*>(lw.s_down[e]);
-                    pd.rows[e] = d;
-                }
-                pd.nsrc = S;
-                pd.cols = fe;
-                pd.mode = 2;
-                TRY(pack_into(h, W.sdown, pd));
+                const bool sh = e >= c.n_experts;
+                const int t = e - c.n_experts;
+                TRY(pack_into(h, ge, src_rows({sh ? lw.s_gate[t] : lw.e_gate[e], sh ? lw.s_up[t] : lw.e_up[e]},
+                                              {fe, fe}, d, 1)));
+                TRY(pack_into(h, de, src_rows({sh ? lw.s_down[t] : lw.e_down[e]}, {d}, fe, 0)));
             }
         }
     }
@@ -1040,11 +1009,9 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
         TRY(dalloc_t(h, &h->route_ids, (size_t)kMaxBlock * K));
         TRY(dalloc_t(h, &h->route_gates, (size_t)kMaxBlock * K));
         TRY(dalloc_t(h, &h->forced, (size_t)c.n_layers * kMaxBlock * K));
-        TRY(dalloc_t(h, &h->y_slot, (size_t)kMaxBlock * K * d));
-        TRY(dalloc_t(h, &h->ys, (size_t)kMaxBlock * d));
-        TRY(dalloc_t(h, &h->xs, (size_t)(std::max(S, 1) * fe / kKBlock) * kStageXBytes));
+        TRY(dalloc_t(h, &h->y_slot, (size_t)kMaxBlock * (K + S) * d));
         h->xe_stride = (long long)(fe / kKBlock) * kStageXBytes;
-        TRY(dalloc_t(h, &h->xe, (size_t)h->xe_stride * kMaxBlock * K));
+        TRY(dalloc_t(h, &h->xe, (size_t)h->xe_stride * (kMaxBlock * K + S)));
     }
     TRYCU(cudaStreamSynchronize(h->stream));
     TRYCU(cudaGetLastError());

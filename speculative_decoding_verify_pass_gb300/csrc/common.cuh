@@ -22,6 +22,7 @@ constexpr int kPageSize = 64;        // KV positions per page
 constexpr int kAttnChunk = 128;      // positions per attention work item
 constexpr int kMaxExperts = 64;
 constexpr int kMaxTopK = 8;
+constexpr int kMaxShared = 2;       // shared experts per MoE layer
 
 // Device state: cache lengths and the last verify's outcome.  Kernels read
 // positions from here, so one launch sequence serves every step.

@@ -15,7 +15,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kThreads = kConsumers + 64;  // + one producer warp + one operand-converter warp
 constexpr int kCsLd = 20;  // padded row stride of the fp32 tile
-constexpr int kMaxItems = kMaxBlock * kMaxTopK;
+constexpr int kMaxItems = kMaxBlock * kMaxTopK + kMaxShared;
 constexpr int kPartFloats = kTileRows * kMaxBlock;
 constexpr int kMaxContrib = 160;  // CTAs that can share one tile (the host caps the grid at 159 per tile)
 
@@ -93,7 +93,18 @@ struct StageIter {
 // The expert work list of one launch, built by all `nthreads` threads of the
 // CTA (call before any role split; contains CTA barriers).  Per slot: item
 // j*k + s is token j's s-th expert.  Dedup: one item per distinct expert in
-// ascending id, with the tokens that route to it and their slots.
+// ascending id, with the tokens that route to it and their slots.  In both
+// modes the shared experts follow as one item each (expert n_experts + t,
+// every token, output slot k + t), read once per launch.
+__device__ __forceinline__ void add_shared_items(const GemmParams& p, GemmSmem& sm, int first) {
+    for (int t = 0; t < p.n_shared; ++t) {
+        Item& it = sm.items[first + t];
+        it.expert = p.n_experts + t;
+        it.mask = (1 << p.n) - 1;
+        for (int j = 0; j < kMaxBlock; ++j) it.slot[j] = j < p.n ? (signed char)(p.top_k + t) : (signed char)-1;
+    }
+}
+
 __device__ __forceinline__ void build_items(const GemmParams& p, GemmSmem& sm, int tid, int nthreads) {
     const int n = p.n, k = p.top_k, nk = n * k;
     int* ids = sm.slots;                  // the block's routing, [n][k] (<= 96 entries)
@@ -108,7 +119,10 @@ __device__ __forceinline__ void build_items(const GemmParams& p, GemmSmem& sm, i
             for (int t = 0; t < kMaxBlock; ++t) it.slot[t] = -1;
             it.slot[j] = (signed char)(i % k);
         }
-        if (tid == 0) sm.n_items = nk;
+        if (tid == 0) {
+            add_shared_items(p, sm, nk);
+            sm.n_items = nk + p.n_shared;
+        }
         return;
     }
     for (int e = tid; e < kMaxExperts; e += nthreads) {   // tokens routed to expert e
@@ -132,7 +146,8 @@ __device__ __forceinline__ void build_items(const GemmParams& p, GemmSmem& sm, i
     if (tid == 0) {
         int cnt = 0;
         for (int e = 0; e < kMaxExperts; ++e) cnt += sm.emask[e] != 0;
-        sm.n_items = cnt;
+        add_shared_items(p, sm, cnt);
+        sm.n_items = cnt + p.n_shared;
     }
 }
 
@@ -350,7 +365,7 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
             const int j = job >> 7, r = job & 127;
             const int R = tile * kTileRows + r;
             if (((it.mask >> j) & 1) && R < p.N)
-                p.y_slot[((size_t)j * p.top_k + it.slot[j]) * p.d + R] = cs[r * kCsLd + j];
+                p.y_slot[((size_t)j * (p.top_k + p.n_shared) + it.slot[j]) * p.d + R] = cs[r * kCsLd + j];
         }
     } else if constexpr (EPI == EPI_STORE) {
         for (int job = tid; job < kTileRows * p.n; job += kConsumers) {

@@ -91,12 +91,13 @@ struct GemmParams {
     int* amax_idx;
     // EPI_ROUTER / experts
     int n_experts, top_k;
+    int n_shared;              // shared experts: work items n_experts.. of every expert launch, all tokens
     int* route_ids;            // [16][top_k]
     float* route_gates;
     const int* forced_ids;     // [16][top_k] or null
     int* debug_ids;            // [n][top_k] or null
     int moe_mode;
-    float* y_slot;             // [16][top_k][d]
+    float* y_slot;             // [16][top_k + n_shared][d]
     float* y_store;            // [16][N] (EPI_STORE)
     uint8_t* xe;               // expert-down operands [item][KBs_down][2 KB]
     long long xe_stride;
@@ -142,12 +143,11 @@ struct EmbedParams {
 };
 cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl);
 
-struct CombineParams {           // MoE: x += sum_s gate*y_slot + y_shared
+struct CombineParams {           // MoE: x += sum_s gate*y_slot[s] + sum_t y_slot[top_k + t]
     float* x;
-    const float* y_slot;
-    const float* y_shared;
+    const float* y_slot;       // [16][top_k + n_shared][d]
     const float* gates;
-    int n, d, top_k;
+    int n, d, top_k, n_shared;
     const uint16_t* g_next;
     uint8_t* xf_out;
     float* ss_out;
@@ -200,9 +200,9 @@ cudaError_t launch_rollback(DevState* st, int which, int new_len, cudaStream_t s
 struct PackSrc {
     const uint16_t* src[4];
     int rows[4];               // rows of each source
-    int cols;                  // K of each source (mode 2: columns per source)
+    int cols;                  // K of each source
     int nsrc;
-    int mode;                  // 0 row concat, 1 gate/up interleave by 64, 2 column concat
+    int mode;                  // 0 row concat, 1 gate/up interleave by 64
 };
 cudaError_t launch_pack(const PackSrc& s, const PackedMat& m, cudaStream_t st);
 

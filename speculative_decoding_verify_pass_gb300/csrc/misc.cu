@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(256) rows_operand_kernel(const __grid_constant
     if (rg == 0 && j < p.n) p.ss_out[j * (p.d / kTileRows) + tile] = ssum;
 }
 
-// MoE layer output: x[j] += sum_s gate[j][s] * y_slot[j][s] + y_shared[j],
-// slots in rank order, then the next norm's operand and sum-of-squares.
+// MoE layer output: x[j] += sum_s gate[j][s] * y_slot[j][s] (routed slots in
+// rank order) + y_slot[j][top_k] + y_slot[j][top_k + 1] (shared experts, in
+// order), then the next norm's operand and sum-of-squares.
 __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant__ CombineParams p) {
     pdl_wait();
     pdl_launch_dependents();
@@ -120,35 +121,38 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(const __grid_constant_
         float* xr = p.x + (size_t)j * p.d + R0;
         // all slot rows at once (independent loads), then the sum in slot order
         float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float4 ys[kMaxTopK][2];
+        const int slots = p.top_k + p.n_shared;
+        float4 ys[kMaxTopK + kMaxShared][2];
         float gs[kMaxTopK];
 #pragma unroll
-        for (int s = 0; s < kMaxTopK; ++s) {
-            if (s < p.top_k) {
-                const float* src = p.y_slot + ((size_t)j * p.top_k + s) * p.d + R0;
+        for (int s = 0; s < kMaxTopK + kMaxShared; ++s) {
+            if (s < slots) {
+                const float* src = p.y_slot + ((size_t)j * slots + s) * p.d + R0;
                 ys[s][0] = *reinterpret_cast<const float4*>(src);
                 ys[s][1] = *reinterpret_cast<const float4*>(src + 4);
-                gs[s] = p.gates[j * p.top_k + s];
             }
+            if (s < kMaxTopK && s < p.top_k) gs[s] = p.gates[j * p.top_k + s];
         }
+        // routed slots weighted by their gates, then the shared experts' slots
 #pragma unroll
-        for (int s = 0; s < kMaxTopK; ++s) {
-            if (s < p.top_k) {
+        for (int s = 0; s < kMaxTopK + kMaxShared; ++s) {
+            if (s < slots) {
                 const float a[8] = {ys[s][0].x, ys[s][0].y, ys[s][0].z, ys[s][0].w,
                                     ys[s][1].x, ys[s][1].y, ys[s][1].z, ys[s][1].w};
+                if (s < kMaxTopK && s < p.top_k) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] += gs[s] * a[e];
+                    for (int e = 0; e < 8; ++e) y[e] += gs[s < kMaxTopK ? s : 0] * a[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) y[e] += a[e];
+                }
             }
         }
         const float4 x0 = *reinterpret_cast<const float4*>(xr), x1 = *reinterpret_cast<const float4*>(xr + 4);
         const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
         float v[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float t = y[e];
-            if (p.y_shared) t += p.y_shared[(size_t)j * p.d + R0 + e];
-            v[e] = xv[e] + t;
-        }
+        for (int e = 0; e < 8; ++e) v[e] = xv[e] + y[e];
         if (p.tap) {
             float* tr = p.tap + (size_t)j * p.d + R0;
             *reinterpret_cast<float4*>(tr) = make_float4(v[0], v[1], v[2], v[3]);
@@ -254,10 +258,6 @@ __global__ void rollback_kernel(DevState* st, int which, int new_len) {
 // Logical row r of the packed matrix -> source element (or zero).
 __device__ __forceinline__ uint16_t pack_fetch(const PackSrc& s, int N, int r, int k) {
     if (r >= N) return 0;
-    if (s.mode == 2) {  // column concat: k selects the source
-        const int src = k / s.cols;
-        return s.src[src][(size_t)r * s.cols + (k - src * s.cols)];
-    }
     int row = r;
     int first = 0, count = s.nsrc;
     if (s.mode == 1) {  // tile t rows 0..63 = gate rows t*64.., rows 64..127 = up rows t*64..
