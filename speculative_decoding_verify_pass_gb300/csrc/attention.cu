@@ -98,9 +98,12 @@ __global__ void __maxnreg__(192) attn_partial_kernel(const __grid_constant__ Att
 }
 
 // Two rows (query head, token) per CTA, one warp each: the chunk partials
-// of a row merged in chunk order.
+// of a row merged in chunk order.  At most 184 registers a thread, so that a
+// merge CTA (64 threads) fits beside a streaming-GEMM CTA (320 threads at up
+// to 168): the next GEMM's CTAs must find room to prefetch their weights
+// while the merge runs.
 template <int HD>
-__global__ void __launch_bounds__(attn_core::kAttnCombThreads) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+__global__ void __maxnreg__(184) attn_combine_kernel(const __grid_constant__ AttnParams p) {
     long long* tr = (p.trace && blockIdx.x < kTraceCtas && threadIdx.x == 0)
                         ? p.trace + (size_t)(kTraceCtas + blockIdx.x) * 4 : nullptr;
     if (tr) tr[0] = trace_clock();

@@ -296,7 +296,11 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
         const size_t sbase = (size_t)sq * a.n_kv_heads * a.nch * 64;
         const float2* ml = a.part_ml + sbase + (size_t)h * a.nch * 64 + r;
         const float* po = a.part_o + (sbase + (size_t)h * a.nch * 64 + r) * HD + lane * V;
+        // the first kFirst chunks' outputs and row maxima in one sweep of
+        // independent loads (one L2 round trip), later chunks' maxima after;
+        // the row sums are read again below, from lines this sweep brought in
         float ob[kFirst][V];
+        float mf[kFirst];
 #pragma unroll
         for (int t = 0; t < kFirst; ++t) {
             if (t < nc) {
@@ -307,10 +311,14 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
                     const float2 v = *reinterpret_cast<const float2*>(po + (size_t)t * cstride);
                     ob[t][0] = v.x; ob[t][1] = v.y;
                 }
+                mf[t] = ml[(size_t)t * 64].x;
             }
         }
         float M = -1e30f;
-        for (int c0 = 0; c0 < nc; c0 += 8) {   // statistics: eight loads in flight
+#pragma unroll
+        for (int t = 0; t < kFirst; ++t)
+            if (t < nc) M = fmaxf(M, mf[t]);
+        for (int c0 = kFirst; c0 < nc; c0 += 8) {   // longer rows: eight statistics loads in flight
             float m[8];
 #pragma unroll
             for (int t = 0; t < 8; ++t) m[t] = c0 + t < nc ? ml[(size_t)(c0 + t) * 64].x : -1e30f;

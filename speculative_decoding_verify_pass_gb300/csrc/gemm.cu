@@ -52,6 +52,9 @@ constexpr int kGroup = 2;   // ring stages a consumer warp may take at once (4: 
 // --------------------------------------------------------------- kernel ---
 template <int EPI, bool TWO>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+    // work items (expert launches) are a property of the epilogue kind, fixed at
+    // compile time: the dense kernels carry none of the item-list code
+    constexpr bool kItems = EPI == EPI_EXPERT_SWIGLU || EPI == EPI_EXPERT_DOWN;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     GemmSmem& sm = *reinterpret_cast<GemmSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -69,13 +72,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     __syncthreads();
 
-    if (p.items_mode) {  // the work list depends on the router's output
+    if constexpr (kItems) {  // the work list depends on the router's output
         pdl_wait();
         pdl_launch_dependents();
         build_items(p, sm, tid, kThreads);
         __syncthreads();
     }
-    const int n_items = p.items_mode ? sm.n_items : 0;
+    const int n_items = kItems ? sm.n_items : 0;
     const uint32_t xb = x_stage_bytes(p.n, p.x_f32);
     const long long xstride = x_kblock_stride(p.x_f32);
 
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         if (!p.x_f32) return;
         named_bar_sync(2, kConsumers + 32);   // the consumers' rstd is in shared memory
         StageIter it;
-        it.init(p, n_items);
+        it.init(p, n_items, kItems);
         bool aborted = false;
         for (int q = 0; it.valid; ++q) {
             const int s = q % kStages;
@@ -101,17 +104,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         // ---------------- producer: one lane issues every bulk copy ----------------
         if (lane == 0) {
             StageIter it;
-            it.init(p, n_items);
+            it.init(p, n_items, kItems);
             int q = 0;
             bool aborted = false;
             auto w_src = [&](const StageIter& s) {
-                const long long e = p.items_mode ? (long long)sm.items[s.item].expert : 0ll;
+                const long long e = kItems ? (long long)sm.items[s.item].expert : 0ll;
                 return p.W + e * p.w_item_stride + ((long long)s.tile * p.KBs + s.b) * kStageWBytes;
             };
             auto x_src = [&](const StageIter& s) {
                 return p.X + (long long)s.item * p.x_item_stride + (long long)s.b * xstride;
             };
-            if (!p.items_mode) {
+            if constexpr (!kItems) {
                 // weights do not depend on the previous kernel: start streaming them now
                 int pre = 0;
                 int pre_b[kStages];
@@ -148,7 +151,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if constexpr (EPI == EPI_QKV) {
         if (tid == 0) sm.pos0 = p.st->len[p.which];   // published by compute_rstd's barriers
     }
-    if (!p.items_mode) {
+    if constexpr (!kItems) {
         pdl_wait();
         pdl_launch_dependents();
     }
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (tr && tid == 0) tr[1] = trace_clock();
 
     StageIter it;
-    it.init(p, n_items);
+    it.init(p, n_items, kItems);
     // fp32 operands reach the consumers already converted (ready barrier)
     uint64_t* gate = p.x_f32 ? sm.ready : sm.full;
     int q = 0;

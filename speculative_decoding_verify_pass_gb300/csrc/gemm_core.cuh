@@ -51,7 +51,7 @@ struct StageIter {
     int tile, item, b, b1;
     bool valid;
 
-    __device__ bool next_seg() {
+    __device__ __forceinline__ bool next_seg() {
         if (!items) {
             if (it >= end) return false;
             tile = (int)(it / KBs);
@@ -70,10 +70,12 @@ struct StageIter {
         u += step;
         return true;
     }
-    __device__ void init(const GemmParams& p, int n_items) {
+    // items: the launch walks (item, tile) units (expert kinds; the callers
+    // pass a compile-time constant so dense kernels carry no item code)
+    __device__ __forceinline__ void init(const GemmParams& p, int n_items, bool items_mode) {
         T = p.T;
         KBs = p.KBs;
-        items = p.items_mode != 0;
+        items = items_mode;
         if (!items) {
             long long I = (long long)p.T * p.KBs;
             it = (long long)blockIdx.x * I / p.grid;
@@ -85,7 +87,7 @@ struct StageIter {
         }
         valid = next_seg();
     }
-    __device__ void advance() {
+    __device__ __forceinline__ void advance() {
         if (++b >= b1) valid = next_seg();
     }
 };

@@ -98,7 +98,7 @@ struct PhaseIter {
         valid = false;
         if (kind == PH_GEMM) {
             if ((int)blockIdx.x < D.g.grid) {
-                gi.init(D.g, 0);
+                gi.init(D.g, 0, false);   // dense phases only
                 valid = gi.valid;
             }
         } else if (kind == PH_ATTN) {
@@ -160,7 +160,7 @@ __device__ void gemm_phase(const GemmParams& gp, PassSmem& sm, int& q, bool& abo
     if ((int)blockIdx.x >= gp.grid) return;
     const int warp = tid >> 5, lane = tid & 31;
     StageIter it;
-    it.init(gp, 0);
+    it.init(gp, 0, false);
     const bool two = gp.n > 8;
     const bool f32 = gp.x_f32 != 0;
     const float ra0 = sm.g.rstd_op[lane >> 2], ra1 = sm.g.rstd_op[8 + (lane >> 2)];
