@@ -46,7 +46,7 @@ def test_skip_sets_match_hand_worked_table():
         assert keep[0] == 0 and keep[-1] == L - 1       # first and last layers are always kept
 
 
-@pytest.mark.parametrize("n", range(1, 12))
+@pytest.mark.parametrize("n", range(1, 17))
 def test_accept_len_exhaustive(n):
     """All 2^(n-1) match patterns: accept_len is the index of the first mismatch
     (the longest matching prefix), n-1 when every draft matches."""
