@@ -379,6 +379,9 @@ long long* trace_slot(spec_model* h, int kind, int slots = 1) {
 }
 
 spec_status gemm(spec_model* h, const GemmParams& p_in, int layer = -1) {
+    // the GEMM kernels fix the work-item mode by epilogue kind (expert kinds walk item lists)
+    const bool items_kind = p_in.epi == EPI_EXPERT_SWIGLU || p_in.epi == EPI_EXPERT_DOWN;
+    if ((p_in.items_mode != 0) != items_kind) return fail(SPEC_ERR_STATE, "internal: GEMM kind %d with item mode %d", p_in.epi, p_in.items_mode);
     GemmParams p = p_in;
     p.trace = trace_slot(h, p.epi);
     const bool rec = h->profiling;
