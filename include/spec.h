@@ -183,7 +183,8 @@ spec_status spec_kv_rollback(spec_handle h, int32_t which, int32_t new_len);
 
 /* MoE expert-read mode: SPEC_MOE_PER_SLOT (one read per token and slot) or
  * SPEC_MOE_DEDUP (one read per distinct expert per pass).  Both give
- * bitwise identical outputs. */
+ * bitwise identical outputs.  The shared experts are read once per pass in
+ * either mode. */
 spec_status spec_moe_mode(spec_handle h, int32_t mode);
 
 /* Shared prefix cache (next row NEXT-1; LayerSkip summary 4.3.3, "Single KV
@@ -315,7 +316,8 @@ spec_status spec_profile_enable(spec_handle h, int32_t enable);
  * kernels.  Bytes are algorithmic (weights + activation operand + outputs,
  * each once); for expert launches they are the expert bytes the launch
  * requests (one expert per (token, slot) in per-slot mode, one per distinct
- * expert in dedup mode, counted from forced routing ids). */
+ * expert in dedup mode, counted from forced routing ids), plus each shared
+ * expert once. */
 spec_status spec_profile_read(spec_handle h, int32_t kind, double* total_ms, double* total_bytes, int32_t* launches);
 
 /* Benchmark hook.  While enabled, every pass records global-timer stamps
