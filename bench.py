@@ -103,8 +103,13 @@ class ClockSampler:
         self.proc = None
         self.lines = []
 
+    PERIOD_MS = 100
+
     def start(self):
-        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms", "200"]
+        """Start sampling; returns once the first sample has arrived (or after
+        two seconds), so that the timed region that follows is covered."""
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits", "-lms",
+               str(self.PERIOD_MS)]
         if self.gpu_id:
             cmd += ["-i", self.gpu_id]
         try:
@@ -114,36 +119,58 @@ class ClockSampler:
             return
         self._t = threading.Thread(target=self._read, daemon=True)
         self._t.start()
+        t0 = time.time()
+        while not self.lines and time.time() - t0 < 2.0:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, t_begin=None, t_end=None):
+        """Stop sampling and summarise the samples that arrived between
+        t_begin and t_end (host seconds; one period of slack after t_end).
+        With no sample in that window every sample is used, and the line says
+        so."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        time.sleep(0.25)
+        time.sleep(2 * self.PERIOD_MS / 1e3)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 7:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for nm, v in zip(names, parts[3:7]):
-                if v.lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarize_clock_lines(self.lines, t_begin, t_end, self.PERIOD_MS / 1e3)
+
+
+def summarize_clock_lines(lines, t_begin=None, t_end=None, slack=0.05):
+    """Median SM clock, maximum SM clock and the throttle reasons seen, from
+    (arrival time, nvidia-smi csv line) pairs of the fields in
+    ClockSampler.FIELDS, restricted to [t_begin, t_end + slack]."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    parsed = []
+    for t, ln in lines:
+        parts = [x.strip() for x in ln.split(",")]
+        if len(parts) < 7:
+            continue
+        try:
+            sm, mx = float(parts[0]), float(parts[1])
+        except ValueError:
+            continue
+        parsed.append((t, sm, mx, [nm for nm, v in zip(names, parts[3:7]) if v.lower() == "active"]))
+    window = parsed
+    in_region = True
+    if t_begin is not None and t_end is not None:
+        window = [p for p in parsed if t_begin <= p[0] <= t_end + slack]
+        if not window:
+            window, in_region = parsed, False
+    reasons = sorted({r for p in window for r in p[3]})
+    out = {"sm_mhz": float(np.median([p[1] for p in window])) if window else None,
+           "sm_max_mhz": max(p[2] for p in window) if window else None,
+           "reasons": reasons, "samples": len(window)}
+    if not in_region:
+        out["note"] = "no sample inside the timed region; all samples of the run are summarised"
+    return out
 
 
 # ----------------------------------------------------------------------------
@@ -254,15 +281,17 @@ def run_native(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    t_begin = time.time()
     e0.record(stream)
     torch.cuda.nvtx.range_push("timed")      # lets a launch-list capture select exactly these launches
     launches = device_cycles(m, torch, gamma, args.steps, buf, acc_log, args.warmup)
     torch.cuda.nvtx.range_pop()
     e1.record(stream)
     torch.cuda.synchronize()
+    t_end = time.time()
     if dist:
         dist.barrier()
-    clocks = clk.stop()
+    clocks = clk.stop(t_begin, t_end)
     ms = e0.elapsed_time(e1)
     m.check_error()
     accepts = acc_log[args.warmup:total].cpu().numpy()
@@ -430,15 +459,20 @@ def oracle_cycle(orc, tc, dc, plan, gamma, ctx, y):
     return k + 1
 
 
-def cpu_baseline(cfg, w, plan, args, prompt):
+def cpu_baseline(cfg, w, plan, args, prompt, min_seconds=10.0, max_cycles=30):
+    """The oracle on the host cores: whole cycles of the bench's workload,
+    repeated until about min_seconds of CPU work (a bounded sample)."""
     import oracle
     orc, tc, dc = oracle_cycle_setup(cfg, w, plan, args.ctx)
     t0 = time.perf_counter()
-    toks = oracle_cycle(orc, tc, dc, plan, args.gamma, args.ctx, int(prompt[-1]))
+    toks, cycles = 0, 0
+    while cycles < max_cycles and (cycles == 0 or time.perf_counter() - t0 < min_seconds):
+        toks += oracle_cycle(orc, tc, dc, plan, args.gamma, args.ctx, int(prompt[-1]))
+        cycles += 1
     dt = time.perf_counter() - t0
     return {"value": round(toks / dt, 4), "unit": "tok/s", "cores": oracle.get_threads(), "kind": "oracle",
-            "sample": "one cycle (%d draft passes + verify n=%d) at context %d on synthetic seeded KV, "
-                      "fp32 C oracle, %.1f s" % (args.gamma, args.gamma + 1, args.ctx, dt)}
+            "sample": "%d cycles (each %d draft passes + verify n=%d) at context %d on synthetic seeded KV, "
+                      "fp32 C oracle, %.1f s" % (cycles, args.gamma, args.gamma + 1, args.ctx, dt)}
 
 
 def run_reference(args):
@@ -1179,7 +1213,7 @@ def suite_extras(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--config", default="qwen3-4b")

@@ -51,3 +51,22 @@ def test_trace_breakdown_skips_launches_without_live_ctas_and_uses_entry_when_ne
     assert out["embed"]["ready_to_exit"] == 2.0
     assert out["attn_merge"]["gap"] == 1.0
     assert span == 3.5
+
+
+def test_clock_summary_keeps_only_samples_inside_the_timed_region():
+    line = "{sm}, 2070, 900.5, {hw}, Not Active, Not Active, {cap}"
+    lines = [(0.9, line.format(sm=1200, hw="Not Active", cap="Not Active")),   # before the region
+             (1.1, line.format(sm=2070, hw="Not Active", cap="Active")),
+             (1.2, line.format(sm=2040, hw="Not Active", cap="Not Active")),
+             (1.3, line.format(sm=2070, hw="Not Active", cap="Not Active")),
+             (2.0, line.format(sm=900, hw="Active", cap="Not Active")),        # long after it
+             (2.1, "garbled")]
+    out = bench.summarize_clock_lines(lines, 1.0, 1.25, slack=0.1)
+    assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_summary_falls_back_to_every_sample_and_says_so():
+    line = "2070, 2070, 900.5, Not Active, Not Active, Not Active, Not Active"
+    out = bench.summarize_clock_lines([(5.0, line), (5.1, line)], 1.0, 1.2)
+    assert out["samples"] == 2 and out["sm_mhz"] == 2070.0 and "note" in out
+    assert bench.summarize_clock_lines([], 1.0, 1.2)["sm_mhz"] is None
