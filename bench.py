@@ -94,16 +94,15 @@ def pass_bytes(cfg, n, ctx, plan=None):
 # clocks sampled during the timed region
 # ----------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, gpu_id: str | None):
         self.gpu_id = gpu_id
         self.proc = None
         self.lines = []
-
-    PERIOD_MS = 100
 
     def start(self):
         """Start sampling; returns once the first sample has arrived (or after
@@ -143,21 +142,32 @@ class ClockSampler:
         return summarize_clock_lines(self.lines, t_begin, t_end, self.PERIOD_MS / 1e3)
 
 
+def _sample_time(stamp, arrival):
+    """A sample's own time (nvidia-smi's local-time stamp) as host seconds,
+    else the time its line was read (the pipe may deliver lines late)."""
+    import datetime
+    try:
+        return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    except ValueError:
+        return arrival
+
+
 def summarize_clock_lines(lines, t_begin=None, t_end=None, slack=0.05):
     """Median SM clock, maximum SM clock and the throttle reasons seen, from
     (arrival time, nvidia-smi csv line) pairs of the fields in
-    ClockSampler.FIELDS, restricted to [t_begin, t_end + slack]."""
+    ClockSampler.FIELDS, restricted to samples taken in [t_begin, t_end + slack]."""
     names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
     parsed = []
     for t, ln in lines:
         parts = [x.strip() for x in ln.split(",")]
-        if len(parts) < 7:
+        if len(parts) < 8:
             continue
         try:
-            sm, mx = float(parts[0]), float(parts[1])
+            sm, mx = float(parts[1]), float(parts[2])
         except ValueError:
             continue
-        parsed.append((t, sm, mx, [nm for nm, v in zip(names, parts[3:7]) if v.lower() == "active"]))
+        parsed.append((_sample_time(parts[0], t), sm, mx,
+                       [nm for nm, v in zip(names, parts[4:8]) if v.lower() == "active"]))
     window = parsed
     in_region = True
     if t_begin is not None and t_end is not None:

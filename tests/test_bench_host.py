@@ -53,20 +53,30 @@ def test_trace_breakdown_skips_launches_without_live_ctas_and_uses_entry_when_ne
     assert span == 3.5
 
 
-def test_clock_summary_keeps_only_samples_inside_the_timed_region():
-    line = "{sm}, 2070, 900.5, {hw}, Not Active, Not Active, {cap}"
-    lines = [(0.9, line.format(sm=1200, hw="Not Active", cap="Not Active")),   # before the region
-             (1.1, line.format(sm=2070, hw="Not Active", cap="Active")),
-             (1.2, line.format(sm=2040, hw="Not Active", cap="Not Active")),
-             (1.3, line.format(sm=2070, hw="Not Active", cap="Not Active")),
-             (2.0, line.format(sm=900, hw="Active", cap="Not Active")),        # long after it
-             (2.1, "garbled")]
-    out = bench.summarize_clock_lines(lines, 1.0, 1.25, slack=0.1)
+def _stamp(t):
+    import datetime
+    return datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+
+
+def test_clock_summary_keeps_only_samples_taken_inside_the_timed_region():
+    t0 = 1_800_000_000.0
+    line = "{ts}, {sm}, 2070, 900.5, {hw}, Not Active, Not Active, {cap}"
+    rows = [(-0.1, 1200, "Not Active", "Not Active"),   # before the region
+            (0.1, 2070, "Not Active", "Active"),
+            (0.2, 2040, "Not Active", "Not Active"),
+            (0.3, 2070, "Not Active", "Not Active"),
+            (1.0, 900, "Active", "Not Active")]          # long after it
+    # every line read only at the end (a buffered pipe): the samples' own stamps decide
+    lines = [(t0 + 5.0, line.format(ts=_stamp(t0 + dt), sm=sm, hw=hw, cap=cap)) for dt, sm, hw, cap in rows]
+    lines.append((t0 + 5.0, "garbled"))
+    out = bench.summarize_clock_lines(lines, t0, t0 + 0.25, slack=0.1)
     assert out == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
 
 
-def test_clock_summary_falls_back_to_every_sample_and_says_so():
-    line = "2070, 2070, 900.5, Not Active, Not Active, Not Active, Not Active"
+def test_clock_summary_uses_arrival_time_without_a_stamp_and_falls_back_to_every_sample():
+    line = "n/a, 2070, 2070, 900.5, Not Active, Not Active, Not Active, Not Active"
+    out = bench.summarize_clock_lines([(1.1, line), (1.15, line), (3.0, line)], 1.0, 1.2)
+    assert out["samples"] == 2 and "note" not in out
     out = bench.summarize_clock_lines([(5.0, line), (5.1, line)], 1.0, 1.2)
     assert out["samples"] == 2 and out["sm_mhz"] == 2070.0 and "note" in out
     assert bench.summarize_clock_lines([], 1.0, 1.2)["sm_mhz"] is None
