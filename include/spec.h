@@ -187,7 +187,7 @@ spec_status spec_kv_rollback(spec_handle h, int32_t which, int32_t new_len);
  * either mode. */
 spec_status spec_moe_mode(spec_handle h, int32_t mode);
 
-/* Shared prefix cache (next row NEXT-1; LayerSkip summary 4.3.3, "Single KV
+/* Shared prefix cache (LayerSkip summary, section 4.3.3, "Single KV
  * Cache").  The draft plan's leading layers 0..E-1 (E = the length of its
  * contiguous prefix 0, 1, 2, ...) compute exactly what the target computes
  * for the same tokens, so with enable != 0 the draft uses the target's KV
@@ -240,8 +240,9 @@ spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, f
 spec_status spec_set_context_fc(spec_handle h, const uint16_t* d_fc, int32_t n_in);
 spec_status spec_context_append(spec_handle h, const float* d_taps, int32_t m);
 
-/* Batched sequences (next row NEXT-3; the pages name several sequences per
- * pass as a way to raise flops per weight byte).  One pass verifies the
+/* Batched sequences (LayerSkip summary, "Critical Assessment": in batched
+ * inference one verify pass serves several sequences, which raises the
+ * flops per weight byte read).  One pass verifies the
  * blocks of nseq independent sequences: every weight is read once for all
  * nseq * n rows, while each sequence attends only to its own cache.
  *

@@ -1,6 +1,7 @@
 """Batched sequences: one verify pass over the blocks of several independent
-sequences, each with its own cache (the pages name several sequences per
-pass as the way to raise flops per weight byte).
+sequences, each with its own cache (LayerSkip summary, "Critical
+Assessment": in batched inference one verify pass serves several sequences,
+which raises the flops per weight byte read).
 
 Every sequence's rows must equal, bit for bit, a single-sequence verify of
 the same block on the same cache (the GEMM columns, attention units and
