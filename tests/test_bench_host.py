@@ -80,3 +80,26 @@ def test_clock_summary_uses_arrival_time_without_a_stamp_and_falls_back_to_every
     out = bench.summarize_clock_lines([(5.0, line), (5.1, line)], 1.0, 1.2)
     assert out["samples"] == 2 and out["sm_mhz"] == 2070.0 and "note" in out
     assert bench.summarize_clock_lines([], 1.0, 1.2)["sm_mhz"] is None
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) on the tiny
+    shape: one JSON line with the contract's keys, its own cpu_baseline and
+    an e2e entry that moves no bytes."""
+    import json
+    import subprocess
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                          "--ctx", "128", "--steps", "2", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tok/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
