@@ -225,7 +225,8 @@ spec_status validate_config(const spec_model_config* c) {
     if (c->n_experts > 0) {
         if (c->top_k < 1 || c->top_k > kMaxTopK || c->top_k > c->n_experts) return fail(SPEC_ERR_INVALID_ARG, "top_k must be in 1..min(8, n_experts)");
         if (c->expert_ffn < 64 || c->expert_ffn % 64) return fail(SPEC_ERR_INVALID_ARG, "expert_ffn must be a positive multiple of 64");
-        if (c->n_shared_experts < 0 || c->n_shared_experts > 2) return fail(SPEC_ERR_INVALID_ARG, "n_shared_experts must be 0..2");
+        if (c->n_shared_experts < 0 || c->n_shared_experts > kMaxShared)
+            return fail(SPEC_ERR_INVALID_ARG, "n_shared_experts must be 0..%d", kMaxShared);
         if (c->first_moe_layer < 0) return fail(SPEC_ERR_INVALID_ARG, "first_moe_layer must be >= 0");
     }
     return SPEC_OK;
