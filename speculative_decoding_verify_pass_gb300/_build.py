@@ -42,14 +42,17 @@ def _stale() -> bool:
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if not force and not _stale():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    # objects in a directory of this process: ranks that build at the same
+    # time never write one another's files; the library is replaced atomically
+    objdir = os.path.join(BUILD, "pid%d" % os.getpid())
+    os.makedirs(objdir, exist_ok=True)
     cc = nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", CSRC,
                     "-I", os.path.join(ROOT, "include"), "--expt-relaxed-constexpr"] + list(extra_flags or [])
     procs = []
     objs = []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc] + flags + ["-c", os.path.join(CSRC, src), "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -70,6 +73,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
     os.replace(tmp, LIB)
+    shutil.rmtree(objdir, ignore_errors=True)
     return LIB
 
 
