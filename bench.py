@@ -480,9 +480,28 @@ def cpu_baseline(cfg, w, plan, args, prompt, min_seconds=10.0, max_cycles=30):
         toks += oracle_cycle(orc, tc, dc, plan, args.gamma, args.ctx, int(prompt[-1]))
         cycles += 1
     dt = time.perf_counter() - t0
-    return {"value": round(toks / dt, 4), "unit": "tok/s", "cores": oracle.get_threads(), "kind": "oracle",
+    cores = oracle.get_threads()
+    return {"value": round(toks / dt, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
             "sample": "%d cycles (each %d draft passes + verify n=%d) at context %d on synthetic seeded KV, "
-                      "fp32 C oracle, %.1f s" % (cycles, args.gamma, args.gamma + 1, args.ctx, dt)}
+                      "fp32 C oracle, %.1f s" % (cycles, args.gamma, args.gamma + 1, args.ctx, dt),
+            "verify_pass_ms": oracle_verify_ms(orc, tc, args.gamma + 1, args.ctx, prompt, cores)}
+
+
+def oracle_verify_ms(orc, tc, n, ctx, prompt, cores):
+    """One verify pass of n tokens at context ctx on the oracle, wall clock,
+    on all the host's cores and on one core."""
+    import oracle
+    block = [int(t) for t in prompt[:n]]
+    out = {}
+    for label, threads in (("all_cores", cores), ("one_core", 1)):
+        oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        orc.forward(tc, orc.full_plan, block, ctx)
+        out[label] = round((time.perf_counter() - t0) * 1e3, 1)
+        tc.truncate(ctx)
+    oracle.set_threads(cores)
+    out["cores"] = cores
+    return out
 
 
 def run_reference(args):
