@@ -59,6 +59,10 @@ def test_argument_errors_need_no_device(lib):
     assert b"multiple of 128" in L.spec_last_error()
     bad = sv._config_c(synth.scaled(synth.tiny(), head_dim=96))
     assert L.spec_model_create(ctypes.byref(bad), None, None, 0, None, ctypes.byref(h)) == sv.SPEC_ERR_INVALID_ARG
+    # the expert kernels hold at most two shared experts per MoE layer as work items
+    bad = sv._config_c(synth.scaled(synth.moe_v2lite(), n_shared_experts=3))
+    assert L.spec_model_create(ctypes.byref(bad), None, None, 0, None, ctypes.byref(h)) == sv.SPEC_ERR_INVALID_ARG
+    assert b"n_shared_experts must be 0..2" in L.spec_last_error()
 
 
 def test_layer_skip_plan_matches_hand_worked_table():
