@@ -305,6 +305,113 @@ def test_first_token_forward_matches_library_path(make):
         assert np.mean(err) < 2e-3 * scale
 
 
+def _rope64(v, pos, theta):
+    """Rotate-half RoPE of head vectors v [..., hd] at `pos`, angles in float64."""
+    hd = v.shape[-1]
+    half = hd // 2
+    ang = pos * theta ** (-2.0 * np.arange(half) / hd)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = v[..., :half], v[..., half:]
+    return np.concatenate([a * c - b * s, b * c + a * s], axis=-1)
+
+
+def _ref_prompt_logits(cfg, w, tokens, rope_q=True, rope_k=True, causal=True):
+    """Logits of every position of a prompt run from an empty cache, by
+    float64 library matmuls with the oracle's bf16 rounding points: q and k
+    rotated at their positions, then rounded; v rounded; query i attends to
+    keys 0..i with softmax(q.k / sqrt(hd)); the attention output rounded.
+    The switches plant wiring mistakes (RoPE left off q or k, attention over
+    every key of the prompt) for the sensitivity checks."""
+    d, eps, hd = cfg.d_model, cfg.norm_eps, cfg.head_dim
+    T = len(tokens)
+    group = cfg.n_heads // cfg.n_kv_heads
+    X = np.stack([widen(w.embed[t]) for t in tokens])
+
+    def norm(v, g):
+        return bf16_np(v / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + eps) * widen(g))
+
+    def ffn(h, wg, wu, wd):
+        g = h @ widen(wg).T
+        u = h @ widen(wu).T
+        return bf16_np(g / (1 + np.exp(-g)) * u) @ widen(wd).T
+
+    for l, L in enumerate(w.layers):
+        H = norm(X, L["attn_norm"])
+        q = (H @ widen(L["wq"]).T).reshape(T, cfg.n_heads, hd)
+        k = (H @ widen(L["wk"]).T).reshape(T, cfg.n_kv_heads, hd)
+        v = bf16_np(H @ widen(L["wv"]).T).reshape(T, cfg.n_kv_heads, hd)
+        for t in range(T):
+            if rope_q:
+                q[t] = _rope64(q[t], t, cfg.rope_theta)
+            if rope_k:
+                k[t] = _rope64(k[t], t, cfg.rope_theta)
+        q, k = bf16_np(q), bf16_np(k)
+        att = np.zeros((T, cfg.n_heads, hd))
+        for t in range(T):
+            keys = t + 1 if causal else T
+            for hh in range(cfg.n_heads):
+                kv = hh // group
+                sc = k[:keys, kv] @ q[t, hh] / np.sqrt(hd)
+                p = np.exp(sc - sc.max())
+                att[t, hh] = bf16_np(p @ v[:keys, kv] / p.sum())
+        X = X + att.reshape(T, -1) @ widen(L["wo"]).T
+        H = norm(X, L["ffn_norm"])
+        if cfg.is_moe_layer(l):
+            Y = np.zeros_like(X)
+            for t in range(T):
+                lg = widen(L["router"]) @ H[t]
+                p = np.exp(lg - lg.max())
+                p /= p.sum()
+                ids = sorted(range(cfg.n_experts), key=lambda e: (-p[e], e))[:cfg.top_k]
+                Y[t] = sum(p[e] * ffn(H[t], L["e_gate"][e], L["e_up"][e], L["e_down"][e]) for e in ids)
+                Y[t] += sum(ffn(H[t], L["s_gate"][s], L["s_up"][s], L["s_down"][s])
+                            for s in range(cfg.n_shared_experts))
+            X = X + Y
+        else:
+            X = X + ffn(H, L["w_gate"], L["w_up"], L["w_down"])
+    return norm(X, w.final_norm) @ widen(w.lm_head_or_embed()).T
+
+
+def _sharpened(cfg, w, factor=6.0):
+    """The same weights with Wq and Wk scaled (then rounded to bf16) so that
+    attention scores spread over several units: softmax is then far from
+    uniform and which keys a query sees, and at which rotation, moves the
+    output at the scale of the logits themselves."""
+    import copy
+    w2 = copy.copy(w)
+    w2.layers = []
+    for L in w.layers:
+        L2 = dict(L)
+        for key in ("wq", "wk"):
+            f = np.asarray(bf16_np(widen(L[key]) * factor), dtype=np.float32)
+            L2[key] = (f.view(np.uint32) >> 16).astype(np.uint16)
+        w2.layers.append(L2)
+    return w2
+
+
+@pytest.mark.parametrize("make", ["tiny", "gqa", "moe"])
+def test_prompt_forward_matches_library_path_at_later_positions(make):
+    """Every position of a 6-token prompt (RoPE on q and k at positions
+    1..5, causal multi-key grouped attention) against the float64 library
+    path, with the same bounds as the position-0 pin.  The library path with
+    RoPE left off q, off k, or with the causal mask dropped lands far outside
+    those bounds, so each of those wiring mistakes in the oracle would fail
+    here."""
+    cfg = {"tiny": synth.tiny(), "gqa": small_gqa_cfg(), "moe": small_moe_cfg()}[make]
+    w = _sharpened(cfg, synth.make_weights(cfg))
+    orc = oracle.Oracle(cfg, w)
+    toks = [int(t) for t in synth.prompt(cfg, 6, stream=31)]
+    lg, _, _ = orc.forward(orc.new_cache(), orc.full_plan, toks, 0, logits_from=0)
+    ref = _ref_prompt_logits(cfg, w, toks)
+    scale = np.max(np.abs(ref))
+    err = np.abs(lg - ref)
+    assert np.max(err) < 2e-2 * scale and np.mean(err) < 2e-3 * scale, (make, np.max(err), np.mean(err), scale)
+    for mutant in (dict(rope_q=False), dict(rope_k=False), dict(causal=False)):
+        bad = _ref_prompt_logits(cfg, w, toks, **mutant)
+        e = np.abs(bad - ref)[1:]          # position 0 is unaffected by all three
+        assert np.mean(e) > 10 * 2e-3 * scale, (make, mutant, np.mean(e), scale)
+
+
 @pytest.mark.parametrize("make", ["tiny", "gqa", "moe"])
 def test_hidden_states_match_library_path(make):
     """The residual stream after every layer (the target hidden states the
