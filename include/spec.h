@@ -275,6 +275,13 @@ const char* spec_last_error(void);
 
 /* ---- inspection, test and benchmark calls ---- */
 
+/* spec_draft_step that also writes the draft's logits: d_logits_opt NULL or
+ * [n][vocab] float32, row i the logits of d_tokens[i] after the kept layers,
+ * the final norm and the LM head (the row whose argmax spec_draft_step
+ * returns is the last).  Same arguments, errors and state change otherwise. */
+spec_status spec_draft_step_logits(spec_handle h, const int32_t* d_tokens, int32_t n, int32_t* d_draft_token,
+                                   float* d_logits_opt);
+
 /* Synchronise the stream and report a device-side error recorded by a
  * bounded wait (SPEC_ERR_TIMEOUT) or a CUDA error. */
 spec_status spec_check_error(spec_handle h);
@@ -360,8 +367,9 @@ spec_status spec_trace_kinds(spec_handle h, int32_t* out, int32_t capacity, int3
  * Scratch: a fixed 128 KB array inside the library, which every GPU that
  * loads the library holds until the process exits; no cudaMalloc, cudaFree or
  * allocating library routine is called.  The first call on a device looks up
- * that array's device address with the device current, so make the first call
- * on each device before any stream capture.  All calls on a device share the
+ * that array's device address with the device current (and so does the first
+ * call after a device reset, which gives the device a new context), so make
+ * the first call on each device before any stream capture.  All calls on a device share the
  * array: calls whose kernels can overlap on the GPU (different streams with
  * no ordering between them) race; calls on one stream are ordered and safe.
  * Each call overwrites every scratch entry it reads, so nothing has to start

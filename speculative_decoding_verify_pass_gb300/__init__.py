@@ -29,7 +29,7 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds",
             "spec_set_taps", "spec_set_context_fc", "spec_context_append", "spec_batch_reserve",
             "spec_batch_kv_load", "spec_batch_kv_export", "spec_batch_set_len", "spec_batch_len",
-            "spec_verify_batch", "spec_share_prefix"]
+            "spec_verify_batch", "spec_share_prefix", "spec_draft_step_logits"]
 
 
 class SpecError(RuntimeError):
@@ -80,6 +80,7 @@ def library():
         "spec_set_stream": [vp, vp],
         "spec_prefill": [vp, vp, i32, vp],
         "spec_draft_step": [vp, vp, i32, vp],
+        "spec_draft_step_logits": [vp, vp, i32, vp, vp],
         "spec_verify_step": [vp, vp, i32, vp, vp, vp, vp, vp],
         "spec_kv_rollback": [vp, i32, i32],
         "spec_moe_mode": [vp, i32],
@@ -141,6 +142,11 @@ def spec_prefill(h, d_tokens, d_next_token):
 
 def spec_draft_step(h, d_tokens, d_draft_token):
     _check(library().spec_draft_step(h, _ptr(d_tokens), int(d_tokens.numel()), _ptr(d_draft_token)))
+
+
+def spec_draft_step_logits(h, d_tokens, d_draft_token, d_logits=None):
+    _check(library().spec_draft_step_logits(h, _ptr(d_tokens), int(d_tokens.numel()), _ptr(d_draft_token),
+                                            _ptr(d_logits)))
 
 
 def spec_verify_step(h, d_block, d_argmax, d_accept_len, d_logits=None, d_expert_ids=None, d_next_pair=None):
@@ -277,8 +283,19 @@ def spec_trace_kinds(h, capacity: int = 4096):
 
 def spec_accept_from_logits_noalloc(d_logits, d_block, d_argmax, d_accept_len, stream=None):
     """Argmax rows and accept_len from caller-computed logits [n][vocab]; the
-    library allocates nothing for this call (fixed in-library scratch)."""
+    library allocates nothing for this call (fixed in-library scratch).
+    d_logits: contiguous float32 CUDA tensor [n][vocab]; d_block, d_argmax:
+    int32 CUDA tensors of at least n entries; d_accept_len: int32, >= 1."""
+    import torch
+    if not (isinstance(d_logits, torch.Tensor) and d_logits.dim() == 2 and d_logits.dtype == torch.float32
+            and d_logits.is_cuda and d_logits.is_contiguous()):
+        raise SpecError(SPEC_ERR_INVALID_ARG, "d_logits must be a contiguous 2-D float32 CUDA tensor")
     n, vocab = int(d_logits.shape[0]), int(d_logits.shape[1])
+    for name, t, need in (("d_block", d_block, n), ("d_argmax", d_argmax, n), ("d_accept_len", d_accept_len, 1)):
+        if not (isinstance(t, torch.Tensor) and t.dtype == torch.int32 and t.is_cuda and t.is_contiguous()
+                and t.numel() >= need):
+            raise SpecError(SPEC_ERR_INVALID_ARG, "%s must be a contiguous int32 CUDA tensor of at least %d entries"
+                            % (name, need))
     st = _stream() if stream is None else ctypes.c_void_p(stream)
     _check(library().spec_accept_from_logits_noalloc(_ptr(d_logits), n, vocab, _ptr(d_block), _ptr(d_argmax),
                                                      _ptr(d_accept_len), st))
@@ -366,10 +383,16 @@ class Model:
         spec_prefill(self.h, t, nxt)
         return nxt
 
-    def draft_step(self, d_tokens, out=None):
+    def draft_step(self, d_tokens, out=None, logits=False):
+        """Draft token of the last of d_tokens (1 or 2); with logits=True
+        returns (token, logits [n][vocab])."""
         out = self._i32(1) if out is None else out
-        spec_draft_step(self.h, d_tokens, out)
-        return out
+        if not logits:
+            spec_draft_step(self.h, d_tokens, out)
+            return out
+        lg = self._torch.empty((d_tokens.numel(), self.cfg.vocab), dtype=self._torch.float32, device="cuda")
+        spec_draft_step_logits(self.h, d_tokens, out, lg)
+        return out, lg
 
     def verify(self, d_block, logits=False, expert_ids=False, next_pair=None):
         n = d_block.numel()

@@ -1086,13 +1086,19 @@ spec_status spec_prefill(spec_handle h, const int32_t* d_tokens, int32_t m, int3
 }
 
 spec_status spec_draft_step(spec_handle h, const int32_t* d_tokens, int32_t n, int32_t* d_draft_token) {
+    return spec_draft_step_logits(h, d_tokens, n, d_draft_token, nullptr);
+}
+
+spec_status spec_draft_step_logits(spec_handle h, const int32_t* d_tokens, int32_t n, int32_t* d_draft_token,
+                                   float* d_logits_opt) {
     if (!h || !d_tokens || !d_draft_token) return fail(SPEC_ERR_INVALID_ARG, "null argument");
     if (n < 1 || n > 2) return fail(SPEC_ERR_INVALID_ARG, "draft step takes 1 or 2 tokens");
     if (h->plan_draft.empty()) return fail(SPEC_ERR_STATE, "model has no draft plan");
     spec_status s = check_capacity(h, 1, n);
     if (s != SPEC_OK) return s;
     h->launches = 0;
-    s = run_pass(h, 1, d_tokens, n, PASS_DRAFT, nullptr, nullptr, nullptr, nullptr, nullptr, d_draft_token, nullptr);
+    s = run_pass(h, 1, d_tokens, n, PASS_DRAFT, nullptr, nullptr, d_logits_opt, nullptr, nullptr, d_draft_token,
+                 nullptr);
     if (s == SPEC_OK) h->host_len[1] += n;
     return s;
 }

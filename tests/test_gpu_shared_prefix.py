@@ -4,14 +4,31 @@ draft's leading layers use the target's KV cache.
 Self-speculative decoding must stay lossless (equal to plain greedy), give
 the same drafts, accept lengths and final target cache, bit for bit, as
 with separate caches, and the draft's shared slots must be the target's own
-pools."""
+pools.  The emitted tokens and accept lengths are also checked against the
+oracle's plain greedy decoding and its own self-speculative loop over the
+same plan (exact, unless the oracle's greedy run passes a near tie)."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
 from conftest import small_gqa_cfg
-from gpu_common import make_model, torch_cuda
+from gpu_common import TIE_GAP, make_model, torch_cuda
+
+
+def _oracle_greedy_with_margin(orc, prompt, max_new):
+    """The oracle's plain greedy tokens and the smallest top-two logit margin
+    met on the way (below TIE_GAP the GPU may take the other token)."""
+    cache = orc.new_cache()
+    lg, _, _ = orc.forward(cache, orc.full_plan, prompt, 0, logits_from=len(prompt) - 1)
+    out, margin = [], np.inf
+    while True:
+        row = np.sort(lg[-1])
+        margin = min(margin, float(row[-1] - row[-2]))
+        out.append(oracle.argmax(lg[-1]))
+        if len(out) == max_new:
+            return out, margin
+        lg, _, _ = orc.forward(cache, orc.full_plan, [out[-1]], cache.len, logits_from=0)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,6 +66,12 @@ def test_shared_prefix_selfspec_is_lossless_and_equals_separate_caches(cfgname, 
     g.close()
     (oa, aa, na, kva), (ob, ab, nb, kvb) = runs[False], runs[True]
     assert ob == greedy and oa == greedy
+    orc = oracle.Oracle(cfg, w)
+    want, margin = _oracle_greedy_with_margin(orc, prompt, 48)
+    if margin >= TIE_GAP:
+        assert ob == want
+        want_ss, want_acc = oracle.selfspec_generate(orc, plan, prompt, 48, gamma)
+        assert want_ss == want and ab == want_acc
     assert ab == aa and nb == na
     for l in range(cfg.n_layers):
         assert np.array_equal(kva[l][0], kvb[l][0]) and np.array_equal(kva[l][1], kvb[l][1]), l
