@@ -18,7 +18,10 @@ logit comparison; for them two more figures are stored: the share of
 differ, and the largest router-probability difference between the builds
 under that forced routing.  Computed by the CPU oracle only.
 
-    python tests/golden/make_fullsize_floor.py
+    python tests/golden/make_fullsize_floor.py [case ...]
+
+With case names, only those cases are computed and their lines replaced or
+appended; the other lines of the file are kept.
 """
 import os
 import sys
@@ -41,6 +44,8 @@ CASES = [
     ("llama-3.1-8b", "llama-3.1-8b", 0, 4096, 8, 7),
     ("qwen3-8b", "qwen3-8b", 0, 2048, 16, 7),
     ("moe-v2-lite", "moe-v2-lite", 0, 2048, 4, 9),
+    ("llama-3.1-8b-n1", "llama-3.1-8b", 0, 4096, 1, 13),
+    ("moe-v2-lite-n8", "moe-v2-lite", 0, 2048, 8, 15),
 ]
 
 ATOL = RTOL = 2e-2
@@ -98,21 +103,29 @@ def run_case(preset, layers, ctx, n, stream):
     return floor_stats(got, ref), route
 
 
-def main():
+def main(only=None):
     out = os.path.join(HERE, "fullsize_floor.txt")
-    lines = ["# fp32-accumulating oracle vs the fp64-accumulating build, same inputs and rounding points",
-             "# written by make_fullsize_floor.py (CPU oracle only); tolerance %g abs + %g rel" % (ATOL, RTOL),
-             "# name preset layers ctx n stream mean_abs max_abs share_outside route_mismatch route_max_dp"]
+    header = ["# fp32-accumulating oracle vs the fp64-accumulating build, same inputs and rounding points",
+              "# written by make_fullsize_floor.py (CPU oracle only); tolerance %g abs + %g rel" % (ATOL, RTOL),
+              "# name preset layers ctx n stream mean_abs max_abs share_outside route_mismatch route_max_dp"]
+    kept = {}
+    if only and os.path.exists(out):
+        for line in open(out):
+            if line.strip() and line[0] != "#":
+                kept[line.split()[0]] = line.rstrip("\n")
     for name, preset, layers, ctx, n, stream in CASES:
+        if only and name not in only:
+            continue
         t = time.time()
         (mean, mx, share), route = run_case(preset, layers, ctx, n, stream)
         tail = "%.6g %.6g" % route if route else "- -"
-        lines.append("%s %s %d %d %d %d %.6g %.6g %.6g %s" % (name, preset, layers, ctx, n, stream, mean, mx, share,
-                                                              tail))
-        print(lines[-1], "(%.0f s)" % (time.time() - t), flush=True)
+        kept[name] = "%s %s %d %d %d %d %.6g %.6g %.6g %s" % (name, preset, layers, ctx, n, stream, mean, mx, share,
+                                                              tail)
+        print(kept[name], "(%.0f s)" % (time.time() - t), flush=True)
+    order = [c[0] for c in CASES if c[0] in kept]
     with open(out, "w") as f:
-        f.write("\n".join(lines) + "\n")
+        f.write("\n".join(header + [kept[k] for k in order]) + "\n")
 
 
 if __name__ == "__main__":
-    main()
+    main(sys.argv[1:] or None)

@@ -32,6 +32,7 @@ _spec.loader.exec_module(_floor_script)
 
 FLOOR = load_floor()
 DENSE = [k for k, c in FLOOR.items() if c["preset"] != "moe-v2-lite"]
+MOE = [k for k, c in FLOOR.items() if c["preset"] == "moe-v2-lite"]
 
 
 def _config(c):
@@ -81,10 +82,13 @@ def test_dense_fullsize_verify_matches_oracle(case, monkeypatch):
     gc.collect()
 
 
-def test_moe_fullsize_verify_matches_oracle_and_modes_agree():
+@pytest.mark.parametrize("case", MOE)
+def test_moe_fullsize_verify_matches_oracle_and_modes_agree(case):
+    """n = 4, and n = 8 where deduplication reads fewest bytes relative to
+    per-slot; both modes must give the same bits and match the oracle."""
     torch = torch_cuda()
     import speculative_decoding_verify_pass_gb300 as sv
-    c = FLOOR["moe-v2-lite"]
+    c = FLOOR[case]
     ctx, n = c["ctx"], c["n"]
     cfg = _config(c)
     w = synth.make_weights(cfg)
