@@ -12,6 +12,8 @@
 // It performs the same reduction as the accept step of spec_verify_step: the
 // argmax of each logit row (lowest id on ties) and the count of leading
 // drafts that equal the previous row's argmax.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -34,8 +36,44 @@ struct NaPartial {
 // 16 rows x 1024 chunks x 8 bytes = 128 KB, shared by every call on a device.
 static __device__ __align__(256) NaPartial g_noalloc_scratch[kMaxBlock * kNaMaxChunks];
 
+// Per device: the array's device address and the context it was looked up
+// in.  A device reset ends the context; the next call runs in a new one,
+// where the module (and the array) may sit at another address, so a changed
+// context id triggers a fresh lookup.
+struct NaAddr {
+    unsigned long long ctx_id;
+    void* ptr;
+};
 std::mutex g_na_mutex;
-void* g_na_ptr[64] = {nullptr};
+NaAddr g_na_addr[64] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context (driver entry points fetched
+// through the runtime, so the library needs no link against libcuda); 0 if
+// the driver cannot tell, in which case the first address stays in use.
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_cur = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_cur && get_id && get_cur(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS) return id;
+    return 0;
+}
 
 __device__ __forceinline__ void na_better(float& bv, int& bi, float v, int i) {
     if (v > bv || (v == bv && i < bi)) {
@@ -134,19 +172,21 @@ extern "C" spec_status spec_accept_from_logits_noalloc(const float* d_logits, in
     }
     void* scratch = nullptr;
     {
-        // Once per device, with that device current: the array's device
-        // address (its name in host code only stands in for it).
+        // Once per device (and again after a device reset), with that device
+        // current: the array's device address (its name in host code only
+        // stands in for it).
         std::lock_guard<std::mutex> lock(g_na_mutex);
-        if (!g_na_ptr[dev]) {
+        const unsigned long long ctx_id = current_context_id();
+        if (!g_na_addr[dev].ptr || g_na_addr[dev].ctx_id != ctx_id) {
             void* p = nullptr;
             const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
             if (e != cudaSuccess || !p) {
                 set_last_error(cudaGetErrorString(e));
                 return SPEC_ERR_CUDA;
             }
-            g_na_ptr[dev] = p;
+            g_na_addr[dev] = NaAddr{ctx_id, p};
         }
-        scratch = g_na_ptr[dev];
+        scratch = g_na_addr[dev].ptr;
     }
     cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
     const int chunks = (vocab + kNaChunk - 1) / kNaChunk;

@@ -46,6 +46,48 @@ def test_accept_from_logits_noalloc_matches_verify_step():
     m.close()
 
 
+def test_accept_from_logits_noalloc_matches_host_argmax_at_the_vocab_limit():
+    """Logits at the largest vocabulary the fixed scratch holds (2,097,152),
+    with planted ties, against numpy's argmax (first maximum): a tie that
+    straddles the 2048-entry chunk boundary, one between two chunks far apart,
+    one row that is constant, and a maximum in the very last entry.  A second
+    call on a small ragged vocabulary follows, reusing the scratch the first
+    left behind; neither call allocates through torch's allocator."""
+    torch = torch_cuda()
+    import speculative_decoding_verify_pass_gb300 as sv
+    V = 2097152
+    rng = np.random.default_rng(17)
+    lg = rng.standard_normal((5, V)).astype(np.float32)
+    lg[0, 2047] = lg[0, 2048] = 9.0           # tie across the first chunk boundary -> 2047
+    lg[1, 4096] = lg[1, V - 1] = 9.5          # tie between distant chunks -> 4096
+    lg[2, :] = 0.25                           # constant row -> 0
+    lg[3, V - 1] = 12.0                       # maximum in the last entry
+    lg[4, 1_000_003] = 8.0
+    want = [int(np.argmax(r)) for r in lg]
+    assert want == [2047, 4096, 0, V - 1, 1_000_003]
+    cases = [(lg, [7, want[0], want[1], 3, 9]),                 # accepts two drafts
+             (rng.standard_normal((3, 1000)).astype(np.float32), None)]
+    for call, (logits, blk) in enumerate(cases):
+        n = logits.shape[0]
+        host_am = [int(np.argmax(r)) for r in logits]
+        if blk is None:
+            blk = [1] + host_am[:n - 1]                          # accepts every draft
+        want_acc = 0
+        while want_acc < n - 1 and blk[want_acc + 1] == host_am[want_acc]:
+            want_acc += 1
+        d_lg = torch.from_numpy(logits).to("cuda")
+        d_blk = torch.tensor(blk, dtype=torch.int32, device="cuda")
+        out_am = torch.full((n,), -7, dtype=torch.int32, device="cuda")
+        out_acc = torch.full((1,), -7, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        before = torch.cuda.memory_allocated()
+        sv.spec_accept_from_logits_noalloc(d_lg, d_blk, out_am, out_acc)
+        torch.cuda.synchronize()
+        assert torch.cuda.memory_allocated() == before
+        assert out_am.cpu().tolist() == host_am, call
+        assert int(out_acc.item()) == want_acc == (2 if call == 0 else n - 1), call
+
+
 def test_accept_from_logits_noalloc_rejects_sizes_beyond_its_scratch():
     torch = torch_cuda()
     import speculative_decoding_verify_pass_gb300 as sv
@@ -61,3 +103,12 @@ def test_accept_from_logits_noalloc_rejects_sizes_beyond_its_scratch():
         sv.spec_accept_from_logits_noalloc(big, blk[:1], out[:1], acc)
     assert e.value.status == sv.SPEC_ERR_INVALID_ARG
     assert b"2097152" in sv.library().spec_last_error()
+    # the binding refuses buffers the kernels would read or write past
+    for bad in (lg.to(torch.bfloat16), lg.t(), lg.cpu()):
+        with pytest.raises(sv.SpecError) as e:
+            sv.spec_accept_from_logits_noalloc(bad, blk, out, acc)
+        assert e.value.status == sv.SPEC_ERR_INVALID_ARG
+    small = torch.zeros((4, 8), dtype=torch.float32, device="cuda")
+    with pytest.raises(sv.SpecError) as e:
+        sv.spec_accept_from_logits_noalloc(small, blk[:3], out, acc)
+    assert e.value.status == sv.SPEC_ERR_INVALID_ARG
