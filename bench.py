@@ -1,19 +1,32 @@
 """Benchmark of the speculative-decoding verify pass on one GB300 (or N replicas).
 
-One step = one greedy self-speculative cycle of the Qwen3-4B-shaped target
-(random-init bf16 weights, prompt of 2048 random ids): gamma draft steps over
-the middle-skip layer plan (the first with the catch-up pair, n=2), one
-verify pass of n = gamma+1 tokens over all 36 layers with argmax and the
-cumulative-product accept, and the device-side rollback of both caches.
-The loop stays on the device (token ids never visit the host).
+Default step (--workload geometric): one verify cycle of the Llama-3.1-8B-
+shaped target (random-init bf16 weights) at KV context 4096 (seeded
+synthetic keys and values): a block of n tokens (default 8: the last accepted
+token and 7 drafts) through all 32 layers with argmax and the cumulative-
+product accept, then the device-side rollback.  The drafts are seeded
+corruptions of the target's own greedy continuation, each draft clean with
+probability alpha (default 0.7), so acceptance is geometric:
+P(accept_len >= j) = alpha^j.  Which drafts are clean depends only on the
+seeded stream, so the cycle schedule (block start, accept length) is fixed
+before the run and the device's accept lengths are checked against it.  The
+loop stays on the device; each block is copied into the verify's input
+buffer on the device.
+
+--workload selfspec keeps the earlier step: one greedy self-speculative cycle
+of the Qwen3-4B-shaped target at context 2048 (gamma draft steps over the
+middle-skip plan, verify n = gamma+1, accept, rollback of both caches).
 
 Printed JSON line: accepted tokens/s (the MLX post's and the DFlash README's
-throughput metric), the verify pass's time and HBM bandwidth against 8 TB/s,
-a roofline entry for the streaming GEMM (the dominant kernel), an end-to-end
-figure through the host-driven API with pinned host copies, the oracle's
-rate on the host cores, and the SM clocks seen during the timed region.
+throughput metric), the verify pass's time and HBM bandwidth against 8 TB/s
+for every block size up to the headline one, a roofline entry for the
+streaming GEMM (the dominant kernel) from an in-pipeline launch trace, an
+end-to-end figure through the host-driven API with pinned host copies, the
+oracle's rate on the host cores, and the SM clocks seen during the timed
+region.
 
-    python bench.py [--steps K] [--warmup W] [--gamma 3] [--skip 0.5]
+    python bench.py [--steps K] [--warmup W] [--n 8] [--alpha 0.7]
+    python bench.py --workload selfspec [--gamma 3] [--skip 0.5]
     python bench.py --impl reference     # the CPU oracle on the same workload
 """
 from __future__ import annotations
@@ -246,7 +259,379 @@ def device_cycles(m, torch, gamma, steps, buf, acc_log, start_idx):
     return launches
 
 
+# ----------------------------------------------------------------------------
+# Default workload: verify cycles with geometric acceptance (Llama-3.1-8B shape)
+# ----------------------------------------------------------------------------
+def geometric_schedule(n, alpha, count, vocab):
+    """(block start, accept length) of `count` verify cycles of n tokens whose
+    n-1 drafts come from synth.corrupt_drafts (stream = cycle index).  Which
+    drafts stay clean depends only on the seeded stream, not on the tokens,
+    so the accept length (the number of leading clean drafts) of every cycle,
+    and with it where the next block starts, is known before the run."""
+    import synth
+    j, out = 0, []
+    for s in range(count):
+        k = 0
+        if n > 1:
+            dummy = np.zeros(n - 1, dtype=np.int32)
+            clean = synth.corrupt_drafts(dummy, alpha, vocab, stream=s) == dummy
+            while k < n - 1 and clean[k]:
+                k += 1
+        out.append((j, k))
+        j += k + 1
+    return out
+
+
+def geometric_blocks(greedy, sched, n, alpha, vocab):
+    """Blocks [greedy[j]] + corrupt_drafts(greedy[j+1 .. j+n-1]) of the
+    schedule; checks that each accepts exactly its scheduled length."""
+    import synth
+    blocks = np.zeros((len(sched), n), dtype=np.int32)
+    for s, (j, k) in enumerate(sched):
+        truth = np.array(greedy[j + 1:j + n], dtype=np.int32)
+        drafts = synth.corrupt_drafts(truth, alpha, vocab, stream=s) if n > 1 else truth
+        blocks[s, 0] = greedy[j]
+        blocks[s, 1:] = drafts
+        lead = 0
+        while lead < n - 1 and drafts[lead] == truth[lead]:
+            lead += 1
+        assert lead == k, (s, lead, k)
+    return blocks
+
+
+def launch_segments(stamps, kinds):
+    """Split one traced pass ([ctas][launches][entry, ready, work, exit]
+    global-timer stamps) into consecutive per-launch segments: launch i owns
+    the time from the previous launch's last CTA exit (or its own first
+    entry, for the first launch) to its own last CTA exit.  The segments
+    tile the pass, so their sum over any set of launches is at most the pass
+    time.  Returns [(kind, microseconds)] in launch order."""
+    out, prev = [], None
+    for l, kind in enumerate(kinds):
+        s = stamps[:, l, :]
+        live = s[s[:, 0] > 0]
+        if len(live) == 0:
+            continue
+        ex = int(live[:, 3].max())
+        start = int(live[:, 0].min()) if prev is None else prev
+        out.append((int(kind), max(ex - start, 0) / 1e3))
+        prev = ex if prev is None else max(prev, ex)
+    return out
+
+
+GEMM_KINDS = (0, 1, 2, 3)      # QKV, residual (O / down), SwiGLU gate-up, LM head
+
+
+def inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind, reps=3):
+    """The streaming GEMM inside an unbracketed verify pass: algorithmic bytes
+    per pass (from one event-profiled pass) over the GEMM launches' trace
+    segments (launch_segments), averaged over `reps` traced passes."""
+    n = blk.numel()
+    am = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sv.spec_profile_enable(m.h, True)
+    sv.spec_verify_step(m.h, blk, am, ac)
+    sv.spec_kv_rollback(m.h, 0, ctx)
+    per_kind = {k: sv.spec_profile_read(m.h, k) for k in GEMM_KINDS}
+    sv.spec_profile_enable(m.h, False)
+    gbytes = sum(v[1] for v in per_kind.values())
+    glaunch = sum(v[2] for v in per_kind.values())
+    sv.spec_trace_enable(m.h, True)
+    seg_us, span_us = [], []
+    for r in range(reps + 1):
+        sv.spec_verify_step(m.h, blk, am, ac)
+        sv.spec_kv_rollback(m.h, 0, ctx)
+        torch.cuda.synchronize()
+        if r == 0:
+            continue     # the first traced pass warms the direct-launch path
+        segs = launch_segments(sv.spec_trace_read(m.h), sv.spec_trace_kinds(m.h))
+        seg_us.append(sum(t for k, t in segs if k in GEMM_KINDS))
+        span_us.append(sum(t for _, t in segs))
+    sv.spec_trace_enable(m.h, False)
+    gus = float(np.mean(seg_us))
+    achieved = gbytes / (gus * 1e-6) / 1e9
+    return {"kernel": "gemm_kernel (weight-streaming GEMM: QKV, O, gate-up, down, LM head)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "timing": "global-timer launch trace of unbracketed verify passes: each launch owns the time from the "
+                      "previous launch's last CTA exit to its own last CTA exit, so the GEMM segments plus the "
+                      "other launches' segments add up to the traced pass",
+            "launches_per_pass": glaunch, "bytes_per_launch": round(gbytes / max(glaunch, 1)),
+            "avg_launch_us": round(gus / max(glaunch, 1), 2), "gemm_us_per_pass": round(gus, 1),
+            "traced_pass_us": round(float(np.mean(span_us)), 1)}
+
+
 def run_native(args):
+    if args.workload == "selfspec":
+        return run_native_selfspec(args)
+    return run_native_geometric(args)
+
+
+def run_native_geometric(args):
+    import torch
+    import speculative_decoding_verify_pass_gb300 as sv
+    import synth
+    from speculative_decoding_verify_pass_gb300 import stepmodel
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    import __graft_entry__
+    __graft_entry__.build()
+
+    n, alpha, ctx = args.n, args.alpha, args.ctx
+    total = args.warmup + args.steps
+    sched = geometric_schedule(n, alpha, total, synth.PRESETS[args.config]().vocab)
+    span = sched[-1][0] + n + 1                        # positions the cycles advance through
+    cfg = synth.PRESETS[args.config](max_ctx=ctx + span + 64)
+    if args.layers:
+        cfg = synth.scaled(cfg, n_layers=args.layers)
+    t0 = time.time()
+    w = synth.make_weights(cfg)
+    t_gen = time.time() - t0
+    m = sv.Model(cfg, w)
+    load_synthetic_context(m, cfg, [], ctx)
+    m.kv_set_len(sv.SPEC_CACHE_TARGET, ctx)
+    m.check_error()
+    # the target's own greedy continuation of the context (verify passes of one token)
+    y0 = int(synth.prompt(cfg, 1)[0])
+    greedy = [y0]
+    one = torch.zeros(1, dtype=torch.int32, device="cuda")
+    am1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ac1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    while len(greedy) < span:
+        one.fill_(greedy[-1])
+        sv.spec_verify_step(m.h, one, am1, ac1)
+        greedy.append(int(am1.item()))
+    sv.spec_kv_rollback(m.h, sv.SPEC_CACHE_TARGET, ctx)
+    blocks = geometric_blocks(greedy, sched, n, alpha, cfg.vocab)
+    d_blocks = torch.from_numpy(blocks).to("cuda")
+    blk = torch.zeros(n, dtype=torch.int32, device="cuda")
+    am = torch.zeros(n, dtype=torch.int32, device="cuda")
+    acc = torch.zeros(1, dtype=torch.int32, device="cuda")
+    acc_log = torch.zeros(total, dtype=torch.int32, device="cuda")
+
+    def cycles(s0, count):
+        launches = 0
+        for s in range(s0, s0 + count):
+            blk.copy_(d_blocks[s])
+            sv.spec_verify_step(m.h, blk, am, acc)
+            launches += m.launches()
+            acc_log[s:s + 1].copy_(acc)
+            sv.spec_kv_rollback(m.h, sv.SPEC_CACHE_TARGET, -1)
+            launches += m.launches()
+        return launches
+
+    cycles(0, args.warmup)
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        uuid = None
+    clk = ClockSampler(uuid)
+    clk.start()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    e0.record(stream)
+    torch.cuda.nvtx.range_push("timed")      # lets a launch-list capture select exactly these launches
+    launches = cycles(args.warmup, args.steps)
+    torch.cuda.nvtx.range_pop()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    if dist:
+        dist.barrier()
+    clocks = clk.stop(t_begin, t_end)
+    ms = e0.elapsed_time(e1)
+    m.check_error()
+    got = acc_log.cpu().numpy()
+    want = np.array([k for _, k in sched], dtype=np.int32)
+    schedule_ok = bool(np.array_equal(got, want))
+    timed = got[args.warmup:total]
+    tokens = float(np.sum(timed + 1))
+    ctx_end = m.kv_len(sv.SPEC_CACHE_TARGET)
+    step_bytes = float(np.mean([pass_bytes(cfg, n, ctx + j) for j, _ in sched[args.warmup:total]]))
+    if dist:
+        ms, tokens = reduce_over_ranks(dist, ms, tokens, "cuda")
+    value = tokens / (ms / 1e3)
+    us_step = ms * 1e3 / args.steps
+    peak, peak_kind = measured_peaks()
+
+    # ---- verify pass alone, per block size, at context ctx ----
+    sweep = {}
+    for nn in range(1, n + 1):
+        us = _verify_us(torch, sv, m, [int(t) for t in blocks[0, :nn]], ctx)
+        b = pass_bytes(cfg, nn, ctx)
+        e_tok = stepmodel.tokens_per_verify(alpha, nn - 1)
+        sweep[str(nn)] = {"us": round(us, 1), "GBps": round(b / us / 1e3, 1),
+                          "frac_8TBps": round(b / us / 1e3 / NOMINAL_HBM, 3),
+                          "frac_measured_peak": round(b / us / 1e3 / peak, 3),
+                          "expected_tokens": round(e_tok, 3), "expected_tok_s": round(e_tok / us * 1e6, 1)}
+
+    # ---- dominant kernel: the streaming GEMM inside unbracketed passes ----
+    blk.copy_(d_blocks[0])
+    roof = inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind)
+
+    # ---- end to end through the host-driven API (pinned copies each step) ----
+    e2e = run_e2e_geometric(m, torch, sv, blocks, sched, ctx, args)
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s verify cycles at KV context %d (seeded synthetic KV), block n=%d (last accepted "
+                               "token + %d drafts), drafts = seeded corruptions of the target's greedy tokens with "
+                               "geometric acceptance alpha=%.2f; verify + accept + device rollback per step" % (
+                                   cfg.name, ctx, n, n - 1, alpha),
+                   "model": cfg.name + "-shaped, random-init N(0,0.02) bf16" + (
+                       ", first %d layers only" % args.layers if args.layers else ""),
+                   "global_batch": world, "seq_len": ctx, "n": n, "alpha": alpha,
+                   "context_range": [ctx + sched[args.warmup][0], ctx_end],
+                   "l2": "no flush: %.1f GB of weights and KV per step exceed the 129 MB L2" % (step_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "accept_mean": round(float(np.mean(timed)), 4),
+        "accept_schedule_matched": schedule_ok,
+        "verify": {"n": n, "us_per_step": round(us_step, 1), "bytes_per_step": round(step_bytes),
+                   "GBps": round(step_bytes / us_step / 1e3, 1),
+                   "frac_8TBps": round(step_bytes / us_step / 1e3 / NOMINAL_HBM, 3),
+                   "frac_measured_peak": round(step_bytes / us_step / 1e3 / peak, 3), "by_n": sweep},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "weights_gen_s": round(t_gen, 1),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_geometric(cfg, w, sched, args)
+    m.close()
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+def run_e2e_geometric(m, torch, sv, blocks, sched, ctx, args):
+    """The same cycles driven from the host: each step copies its block from
+    pinned host memory to the device, runs the verify, reads the argmax rows
+    and accept_len back into pinned memory, and rolls the cache back with
+    the host's exact length."""
+    n = blocks.shape[1]
+    pin_in = torch.zeros(n, dtype=torch.int32).pin_memory()
+    pin_out = torch.zeros(n + 1, dtype=torch.int32).pin_memory()
+    dev_in = torch.zeros(n, dtype=torch.int32, device="cuda")
+    am = torch.zeros(n, dtype=torch.int32, device="cuda")
+    out = torch.zeros(n + 1, dtype=torch.int32, device="cuda")
+    steps = min(max(3, args.steps), len(sched))
+    host_blocks = torch.from_numpy(blocks)
+    pos = ctx
+    sv.spec_kv_rollback(m.h, 0, pos)
+    tokens, matched = 0, True
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        pin_in.copy_(host_blocks[s])
+        dev_in.copy_(pin_in, non_blocking=True)
+        sv.spec_verify_step(m.h, dev_in, am, out[n:n + 1])
+        out[:n].copy_(am)
+        pin_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        k = int(pin_out[n])
+        matched = matched and k == sched[s][1]
+        sv.spec_kv_rollback(m.h, 0, pos + k + 1)
+        pos += k + 1
+        tokens += k + 1
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": round(tokens / dt, 2), "unit": "tok/s", "h2d_bytes_per_step": 4 * n,
+            "d2h_bytes_per_step": 4 * (n + 1), "steps": steps, "accept_schedule_matched": matched}
+
+
+def oracle_verify_setup(cfg, w, ctx):
+    import oracle
+    import synth
+    orc = oracle.Oracle(cfg, w)
+    tc = orc.new_cache()
+    for l in range(cfg.n_layers):
+        tc.load(l, synth.synthetic_kv(cfg, l, ctx, 0).reshape(ctx, -1),
+                synth.synthetic_kv(cfg, l, ctx, 1).reshape(ctx, -1))
+    tc.set_len(ctx)
+    return orc, tc
+
+
+def cpu_baseline_geometric(cfg, w, sched, args, min_seconds=10.0, max_passes=30):
+    """The oracle on the host cores: verify passes of n tokens at context ctx
+    (the block's token ids from synth.prompt; the time does not depend on
+    them), each credited with the tokens its cycle of the acceptance
+    schedule emits, repeated until about min_seconds of CPU work."""
+    import oracle
+    import synth
+    orc, tc = oracle_verify_setup(cfg, w, args.ctx)
+    block = [int(t) for t in synth.prompt(cfg, args.n, stream=5)]
+    t0 = time.perf_counter()
+    toks, passes = 0, 0
+    while passes < max_passes and (passes == 0 or time.perf_counter() - t0 < min_seconds):
+        orc.forward(tc, orc.full_plan, block, args.ctx)
+        tc.truncate(args.ctx)
+        toks += sched[passes % len(sched)][1] + 1
+        passes += 1
+    dt = time.perf_counter() - t0
+    cores = oracle.get_threads()
+    return {"value": round(toks / dt, 4), "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": "%d verify passes (n=%d, all %d layers, context %d, synthetic seeded KV) of the fp32 C oracle, "
+                      "%.1f s; tokens per pass from the same acceptance schedule as the GPU arm" % (
+                          passes, args.n, cfg.n_layers, args.ctx, dt),
+            "verify_pass_ms": oracle_verify_ms(orc, tc, args.n, args.ctx, block, cores)}
+
+
+def run_reference_geometric(args):
+    import oracle
+    import synth
+    oracle.build()
+    synth.build()
+    total = args.warmup + args.steps
+    sched = geometric_schedule(args.n, args.alpha, total, synth.PRESETS[args.config]().vocab)
+    cfg = synth.PRESETS[args.config](max_ctx=args.ctx + 64)
+    if args.layers:
+        cfg = synth.scaled(cfg, n_layers=args.layers)
+    w = synth.make_weights(cfg)
+    orc, tc = oracle_verify_setup(cfg, w, args.ctx)
+    block = [int(t) for t in synth.prompt(cfg, args.n, stream=5)]
+    for _ in range(args.warmup):
+        orc.forward(tc, orc.full_plan, block, args.ctx)
+        tc.truncate(args.ctx)
+    t0 = time.perf_counter()
+    toks = 0
+    for s in range(args.warmup, total):
+        orc.forward(tc, orc.full_plan, block, args.ctx)
+        tc.truncate(args.ctx)
+        toks += sched[s][1] + 1
+    dt = time.perf_counter() - t0
+    value = toks / dt
+    sample = ("each step one verify pass (n=%d, all %d layers) of the fp32 C oracle at context %d on synthetic seeded "
+              "KV, credited with the tokens of the same geometric acceptance schedule (alpha=%.2f) as the GPU arm" % (
+                  args.n, cfg.n_layers, args.ctx, args.alpha))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tok/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "%s verify cycles at KV context %d, block n=%d, geometric acceptance alpha=%.2f" % (
+            cfg.name, args.ctx, args.n, args.alpha), "seq_len": args.ctx, "n": args.n, "alpha": args.alpha},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tok/s", "cores": oracle.get_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+def run_native_selfspec(args):
     import torch
     import speculative_decoding_verify_pass_gb300 as sv
     import synth
@@ -508,6 +893,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
+    if args.workload != "selfspec":
+        return run_reference_geometric(args)
     import oracle
     import synth
     oracle.build()
@@ -1242,13 +1629,16 @@ def suite_extras(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=60)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--config", default="qwen3-4b")
-    ap.add_argument("--gamma", type=int, default=3)
-    ap.add_argument("--skip", type=float, default=0.5)
-    ap.add_argument("--ctx", type=int, default=2048)
+    ap.add_argument("--workload", default="geometric", choices=["geometric", "selfspec"])
+    ap.add_argument("--config", default=None, help="model preset (default llama-3.1-8b; selfspec: qwen3-4b)")
+    ap.add_argument("--n", type=int, default=8, help="geometric: verify block size (last accepted + n-1 drafts)")
+    ap.add_argument("--alpha", type=float, default=0.7, help="geometric: probability that a draft is clean")
+    ap.add_argument("--gamma", type=int, default=3, help="selfspec: draft steps per cycle")
+    ap.add_argument("--skip", type=float, default=0.5, help="selfspec: middle-skip fraction of the draft")
+    ap.add_argument("--ctx", type=int, default=None, help="KV context (default 4096; selfspec: 2048)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="keep only the first N layers (a smaller case for counter captures; the line names it)")
@@ -1256,6 +1646,10 @@ def main():
                              "selfspec", "trace", "extras"],
                     help="run one measurement suite instead of the default bench line")
     args = ap.parse_args()
+    if args.config is None:
+        args.config = "qwen3-4b" if args.workload == "selfspec" or args.suite else "llama-3.1-8b"
+    if args.ctx is None:
+        args.ctx = 2048 if args.workload == "selfspec" or args.suite else 4096
     if args.suite:
         import __graft_entry__
         __graft_entry__.build()

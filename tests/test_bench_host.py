@@ -103,3 +103,39 @@ def test_reference_arm_prints_one_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_geometric_schedule_accepts_the_clean_prefix_and_advances():
+    """The cycle schedule of the default workload: each cycle's accept length
+    is its number of leading clean drafts (corrupted drafts differ from the
+    truth), the next block starts accept+1 positions later, and over many
+    cycles P(accept >= j) follows alpha^j."""
+    import synth
+    n, alpha, V = 8, 0.7, 128256
+    sched = bench.geometric_schedule(n, alpha, 4000, V)
+    assert sched[0][0] == 0
+    for (j0, k0), (j1, _) in zip(sched, sched[1:]):
+        assert 0 <= k0 <= n - 1 and j1 == j0 + k0 + 1
+    ks = np.array([k for _, k in sched])
+    for j in range(1, n):
+        p = alpha ** j
+        assert abs(np.mean(ks >= j) - p) < 4 * np.sqrt(p * (1 - p) / len(ks)) + 1e-9, j
+    greedy = list(synth.prompt(synth.llama31_8b(), sched[40][0] + n + 1, stream=3))
+    blocks = bench.geometric_blocks(greedy, sched[:40], n, alpha, V)
+    for s, (j, k) in enumerate(sched[:40]):
+        assert blocks[s, 0] == greedy[j]
+        assert list(blocks[s, 1:k + 1]) == greedy[j + 1:j + k + 1]
+        if k < n - 1:
+            assert blocks[s, k + 1] != greedy[j + k + 1]
+
+
+def test_launch_segments_tile_the_pass():
+    st = _stamps([
+        [(0, 1000, 2000, 5000, 6000), (1, 1100, 2100, 5500, 7000)],   # first launch: from its first entry
+        [(0, 6500, 8000, 0, 9000)],                                     # starts before the previous exit
+        [],                                                             # nothing recorded
+        [(3, 9100, 10000, 12000, 13000)],
+    ])
+    segs = bench.launch_segments(st, [0, 16, 1, 3])
+    assert segs == [(0, 6.0), (16, 2.0), (3, 4.0)]
+    assert sum(t for _, t in segs) == (13000 - 1000) / 1e3
