@@ -1530,13 +1530,14 @@ def trace_breakdown(stamps, kinds):
 
 def suite_trace(args):
     """Where a verify pass's time goes: the launch trace (per-CTA global-timer
-    stamps, separate launches) of the Qwen3-4B-shaped verify at context 2048
-    for n = 1, 4, 8, 16, summarised per launch kind."""
+    stamps, separate launches) of a verify pass (--config, --ctx; default the
+    Qwen3-4B shape at context 2048) for n = 1, 4, 8, 16, summarised per
+    launch kind."""
     import torch
     import synth
     import speculative_decoding_verify_pass_gb300 as sv
     ctx = args.ctx
-    cfg = synth.qwen3_4b(max_ctx=ctx + 64)
+    cfg = synth.PRESETS[args.config](max_ctx=ctx + 64)
     m, _ = _model_at_context(cfg, ctx)
     for n in (1, 4, 8, 16):
         toks = synth.prompt(cfg, n).tolist()

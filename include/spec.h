@@ -210,9 +210,7 @@ spec_status spec_share_prefix(spec_handle h, int32_t enable);
  *   d_out   device buffer of count * 16 * d_model floats, 16-byte aligned,
  *           CALLER-owned; it must stay valid while taps are on.
  * Synchronises the stream and drops captured launch sequences.  Errors:
- * SPEC_ERR_INVALID_ARG (range, duplicates, alignment, NULL), state unchanged.
- * Taps run on the separate-launch path (the opt-in persistent pass kernel is
- * not used while they are on). */
+ * SPEC_ERR_INVALID_ARG (range, duplicates, alignment, NULL), state unchanged. */
 spec_status spec_set_taps(spec_handle h, const int32_t* layers, int32_t count, float* d_out);
 
 /* Block-draft conditioning (mlx-dflash README, "Architecture": the target's
@@ -311,43 +309,37 @@ spec_status spec_moe_force_routing(spec_handle h, const int32_t* d_ids);
 /* Number of the library's kernel launches enqueued by the last call. */
 int32_t spec_last_launch_count(spec_handle h);
 
-/* Benchmark hook: while enabled, every streaming-GEMM launch (and every
- * persistent pass kernel) is bracketed by CUDA events on the handle's stream
- * (this serialises those launches with their neighbours).  enable = 0 stops
- * recording. */
+/* Benchmark hook: while enabled, every streaming-GEMM launch is bracketed by
+ * CUDA events on the handle's stream (this serialises those launches with
+ * their neighbours).  enable = 0 stops recording. */
 spec_status spec_profile_enable(spec_handle h, int32_t enable);
 
 /* Synchronise the stream and return, for the recorded launches of one kind:
  * the summed event time in ms, the summed bytes and the launch count, and
  * drop those records.  kind = -1: every dense launch (GEMMs outside the expert
- * FFN, and pass kernels); -2: all; 0..7: one GEMM epilogue kind; 100: pass
- * kernels.  Bytes are algorithmic (weights + activation operand + outputs,
+ * FFN); -2: all; 0..7: one GEMM epilogue kind.  Bytes are algorithmic (weights + activation operand + outputs,
  * each once); for expert launches they are the expert bytes the launch
  * requests (one expert per (token, slot) in per-slot mode, one per distinct
  * expert in dedup mode, counted from forced routing ids), plus each shared
  * expert once. */
 spec_status spec_profile_read(spec_handle h, int32_t kind, double* total_ms, double* total_bytes, int32_t* launches);
 
-/* Benchmark hook.  While enabled, every pass records global-timer stamps
- * (nanoseconds) per CTA:
- *  - the persistent pass kernel, per phase: phase entered, grid barrier
- *    passed, phase work done, last streamed stage consumed (or 0);
- *  - otherwise the pass runs its kernels as separate launches (no graph
- *    replay) and every GEMM and attention launch records, per CTA: entry,
- *    inputs ready (after waiting for the previous kernel), main work done
- *    (GEMM: last weight stage consumed; attention: K/V slabs arrived), exit.
- *    Stamps a kernel has no point for are 0.
+/* Benchmark hook.  While enabled, every pass runs its kernels as separate
+ * launches (no graph replay) and every GEMM and attention launch records
+ * global-timer stamps (nanoseconds) per CTA: entry, inputs ready (after
+ * waiting for the previous kernel), main work done (GEMM: last weight stage
+ * consumed; attention: K/V slabs arrived), exit.  Stamps a kernel has no
+ * point for are 0.
  * Each pass overwrites the previous record.  Allocates the trace buffer on
  * enable; synchronous. */
 spec_status spec_trace_enable(spec_handle h, int32_t enable);
 
 /* Copy the last traced pass's stamps ([nctas][nphase][4]) to the host array
- * out (capacity entries).  nphase is the number of phases (pass kernel) or of
- * traced launches; nctas is the pass kernel's grid, or 512 slots per launch
- * (unused slots hold zeros).  Synchronises the stream. */
+ * out (capacity entries).  nphase is the number of traced launches; nctas is
+ * 512 slots per launch (unused slots hold zeros).  Synchronises the stream. */
 spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int32_t* nphase, int32_t* nctas);
 
-/* Kind of each traced phase or launch of the last traced pass (count
+/* Kind of each traced launch of the last traced pass (count
  * entries): 0..7 the GEMM epilogue kind (0 QKV, 1 residual, 2 SwiGLU, 3 LM
  * head, 4 router, 5 expert gate-up, 6 expert down, 7 store), 16 attention
  * partials, 17 attention chunk merge, 18 embedding, 19 accept. */

@@ -250,7 +250,7 @@ def spec_profile_enable(h, enable: bool):
 
 
 EPI_QKV, EPI_RESID, EPI_SWIGLU, EPI_LMHEAD, EPI_ROUTER, EPI_EXPERT_SWIGLU, EPI_EXPERT_DOWN, EPI_STORE = range(8)
-PROF_DENSE, PROF_ALL, PROF_PASS = -1, -2, 100
+PROF_DENSE, PROF_ALL = -1, -2
 
 
 def spec_profile_read(h, kind: int = PROF_DENSE):

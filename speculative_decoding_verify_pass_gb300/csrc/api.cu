@@ -110,20 +110,10 @@ struct spec_model {
     int host_len[2] = {0, 0};   // upper bounds of the device lengths
     bool len_exact[2] = {true, true};
     int launches = 0;
-    bool use_pass = false;              // persistent pass kernel for dense models (SPEC_PASS_KERNEL=1)
-    int* gbar = nullptr;                // pass kernel's grid-barrier counters
     long long* trace = nullptr;         // phase timestamps of the last traced pass
     size_t trace_cap = 0;
-    int trace_nphase = 0;
-    int trace_mode = 0;                 // 1: pass-kernel phases, 2: separate launches
-    std::vector<int32_t> trace_kinds;   // per traced phase or launch
-    struct PassTable {
-        PhaseDesc* dev;
-        int count;
-        double gemm_bytes;   // algorithmic bytes of the table's GEMM phases
-        std::vector<int32_t> kinds;  // per phase: GEMM epilogue kind, or a kTrace* code
-    };
-    std::map<int, PassTable> tables;   // (which, n, lm) -> device phase list
+    bool tracing = false;               // the current pass records launch stamps
+    std::vector<int32_t> trace_kinds;   // per traced launch
     bool profiling = false;
     bool use_graphs = true;             // replay captured launch sequences (SPEC_GRAPHS=0: direct launches)
     cudaStream_t cap_stream = nullptr;  // private stream used only for capture
@@ -135,7 +125,7 @@ struct spec_model {
     struct ProfRec {
         cudaEvent_t a, b;
         double bytes;
-        int kind;   // EPI_* of a GEMM launch, 100 for a whole pass kernel
+        int kind;   // EPI_* of the GEMM launch
     };
     std::vector<int32_t> forced_host;   // host copy of forced routing ids
     std::vector<ProfRec> prof;
@@ -371,7 +361,7 @@ double expert_launch_bytes(spec_model* h, const GemmParams& p, int layer) {
 
 // Next launch slot of a traced pass (nullptr when not tracing or full).
 long long* trace_slot(spec_model* h, int kind, int slots = 1) {
-    if (!h->trace || h->trace_mode != 2) return nullptr;
+    if (!h->trace || !h->tracing) return nullptr;
     const size_t per = (size_t)kTraceCtas * 4;
     if ((h->trace_kinds.size() + slots) * per > h->trace_cap) return nullptr;
     long long* t = h->trace + h->trace_kinds.size() * per;
@@ -404,10 +394,6 @@ spec_status gemm(spec_model* h, const GemmParams& p_in, int layer = -1) {
 }
 
 // One pass of n tokens through a plan (target: all layers; draft: kept layers).
-spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
-                            int32_t* d_accept, float* d_logits, int32_t* d_pair, int32_t* d_token,
-                            const int32_t* d_block);
-
 spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode,
                             int32_t* d_argmax, int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair,
                             int32_t* d_token, const int32_t* d_block);
@@ -417,15 +403,13 @@ void clear_graphs(spec_model* h) {
     h->graphs.clear();
 }
 
-// One pass: the persistent pass kernel (opt-in, dense), or the per-phase
-// launch sequence, replayed from a captured CUDA graph when possible.
+// One pass: the per-phase launch sequence, replayed from a captured CUDA
+// graph when possible.
 spec_status run_pass(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
                      int32_t* d_accept, float* d_logits, int32_t* d_ids, int32_t* d_pair, int32_t* d_token,
                      const int32_t* d_block) {
-    if (h->use_pass && h->c.n_experts == 0 && h->tap_count == 0 && h->bat_nseq == 0)
-        return run_pass_kernel(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_pair, d_token, d_block);
     if (h->trace) {  // a traced pass runs its launches directly, each with its own stamp slots
-        h->trace_mode = 2;
+        h->tracing = true;
         h->trace_kinds.clear();
         CU(cudaMemsetAsync(h->trace, 0, h->trace_cap * sizeof(long long), h->stream));
         return run_pass_launch(h, which, d_tokens, n, mode, d_argmax, d_accept, d_logits, d_ids, d_pair, d_token,
@@ -657,174 +641,6 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
     return SPEC_OK;
 }
 
-// ---- persistent pass kernel (dense models) ----
-AttnParams attn_params(spec_model* h, int which, int n, uint16_t* kpool, uint16_t* vpool) {
-    AttnParams a{};
-    a.qbuf = h->qbuf;
-    a.kpool = kpool;
-    a.vpool = vpool;
-    a.block_table = h->block_table;
-    a.part_o = h->attn_o;
-    a.part_ml = h->attn_ml;
-    a.xf_out = h->xf_o;
-    a.st = h->st;
-    a.which = which;
-    a.n = n;
-    a.n_heads = h->c.n_heads;
-    a.n_kv_heads = h->c.n_kv_heads;
-    a.head_dim = h->c.head_dim;
-    a.nch = h->nch;
-    a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)h->c.head_dim));
-    return a;
-}
-
-spec_status pass_table(spec_model* h, int which, int n, bool lm, spec_model::PassTable* out) {
-    const int key = which * 10000 + n * 10 + (lm ? 1 : 0);
-    auto f = h->tables.find(key);
-    if (f != h->tables.end()) {
-        *out = f->second;
-        return SPEC_OK;
-    }
-    const spec_model_config& c = h->c;
-    const std::vector<int>& plan = which == 0 ? h->plan_full : h->plan_draft;
-    const int d = c.d_model, G = h->num_sms;
-    std::vector<PhaseDesc> v;
-    auto phase = [&](int kind) -> PhaseDesc& {
-        v.emplace_back();
-        std::memset(&v.back(), 0, sizeof(PhaseDesc));
-        v.back().kind = kind;
-        return v.back();
-    };
-    {
-        PhaseDesc& e = phase(PH_EMBED);
-        e.e.embed = h->embed;
-        e.e.n = n;
-        e.e.d = d;
-        e.e.vocab = c.vocab;
-        e.e.x = h->x;
-        e.e.g_next = h->L[plan[0]].attn_norm;
-        e.e.xf_out = h->xf_norm;
-        e.e.ss_out = h->ss;
-        e.e.st = h->st;
-    }
-    for (size_t si = 0; si < plan.size(); ++si) {
-        const int l = plan[si];
-        LayerW& W = h->L[l];
-        const uint16_t* g_after = (si + 1 < plan.size()) ? h->L[plan[si + 1]].attn_norm : h->final_norm;
-        uint16_t* kpool = kv_pool(h, which, which == 0 ? l : (int)si, 0);
-        uint16_t* vpool = kv_pool(h, which, which == 0 ? l : (int)si, 1);
-        GemmParams p = base_params(h, which, n);
-        set_mat(h, p, W.qkv, h->xf_norm, EPI_QKV, G);
-        p.norm_dim = d;
-        p.rope = h->rope;
-        p.qbuf = h->qbuf;
-        p.kpool = kpool;
-        p.vpool = vpool;
-        p.block_table = h->block_table;
-        phase(PH_GEMM).g = p;
-        phase(PH_ATTN).a = attn_params(h, which, n, kpool, vpool);
-        phase(PH_COMB).a = attn_params(h, which, n, kpool, vpool);
-        p = base_params(h, which, n);
-        set_mat(h, p, W.o, h->xf_o, EPI_RESID, G);
-        p.g_next = W.ffn_norm;
-        p.xf_out = h->xf_norm;
-        phase(PH_GEMM).g = p;
-        p = base_params(h, which, n);
-        set_mat(h, p, W.gu, h->xf_norm, EPI_SWIGLU, G);
-        p.norm_dim = d;
-        p.xf_out = h->xf_down;
-        phase(PH_GEMM).g = p;
-        p = base_params(h, which, n);
-        set_mat(h, p, W.down, h->xf_down, EPI_RESID, G);
-        p.g_next = g_after;
-        p.xf_out = h->xf_norm;
-        phase(PH_GEMM).g = p;
-    }
-    if (lm) {
-        GemmParams p = base_params(h, which, n);
-        set_mat(h, p, h->lm, h->xf_norm, EPI_LMHEAD, G);
-        p.norm_dim = d;
-        p.amax_val = h->amax_val;
-        p.amax_idx = h->amax_idx;
-        phase(PH_GEMM).g = p;
-        phase(PH_ACCEPT);
-    } else {
-        phase(PH_ADVANCE);
-    }
-    PhaseDesc* dev = nullptr;
-    spec_status s = dalloc(h, reinterpret_cast<void**>(&dev), sizeof(PhaseDesc) * v.size());
-    if (s != SPEC_OK) return s;
-    CU(cudaMemcpyAsync(dev, v.data(), sizeof(PhaseDesc) * v.size(), cudaMemcpyHostToDevice, h->stream));
-    CU(cudaStreamSynchronize(h->stream));
-    double gb = 0.0;
-    for (const PhaseDesc& ph : v)
-        if (ph.kind == PH_GEMM) gb += gemm_bytes(ph.g);
-    std::vector<int32_t> kinds;
-    for (const PhaseDesc& ph : v)
-        kinds.push_back(ph.kind == PH_GEMM ? ph.g.epi : ph.kind == PH_ATTN ? kTraceAttnPartial
-                        : ph.kind == PH_COMB ? kTraceAttnCombine : ph.kind == PH_EMBED ? kTraceEmbed
-                        : kTraceAccept);
-    h->tables[key] = {dev, (int)v.size(), gb, kinds};
-    *out = h->tables[key];
-    return SPEC_OK;
-}
-
-spec_status run_pass_kernel(spec_model* h, int which, const int32_t* d_tokens, int n, PassMode mode, int32_t* d_argmax,
-                            int32_t* d_accept, float* d_logits, int32_t* d_pair, int32_t* d_token,
-                            const int32_t* d_block) {
-    const bool lm = mode != PASS_PREFILL_MID;
-    spec_model::PassTable tab{};
-    spec_status s = pass_table(h, which, n, lm, &tab);
-    if (s != SPEC_OK) return s;
-    PassParams P{};
-    P.phases = tab.dev;
-    P.nphase = tab.count;
-    P.n = n;
-    P.which = which;
-    P.mode = mode == PASS_VERIFY ? ACC_VERIFY : (mode == PASS_DRAFT ? ACC_DRAFT : ACC_PREFILL);
-    P.nch = h->nch;
-    P.st = h->st;
-    P.gbar = h->gbar;
-    P.tokens = d_tokens;
-    P.logits = d_logits;
-    P.block = d_block;
-    P.out_argmax = d_argmax;
-    P.out_accept = d_accept;
-    P.out_pair = d_pair;
-    P.out_token = d_token;
-    P.amax_val = h->amax_val;
-    P.amax_idx = h->amax_idx;
-    P.lm_T = h->lm.T;
-    if (h->trace) {
-        const size_t need = (size_t)h->num_sms * tab.count * 4;
-        if (need <= h->trace_cap) {
-            P.trace = h->trace;
-            h->trace_nphase = tab.count;
-            h->trace_mode = 1;
-            h->trace_kinds = tab.kinds;
-        }
-    }
-    spec_model::ProfRec r{};
-    if (h->profiling) {
-        // exact context for the KV bytes (profiling only: synchronises)
-        if ((s = sync_lengths(h)) != SPEC_OK) return s;
-        const size_t layers = which == 0 ? h->plan_full.size() : h->plan_draft.size();
-        const double kv = (double)layers * 2.0 * h->c.n_kv_heads * h->c.head_dim * 2.0 * (h->host_len[which] + n);
-        r.bytes = tab.gemm_bytes + kv + (double)n * h->c.d_model * 2.0;
-        r.kind = 100;
-        CU(cudaEventCreate(&r.a));
-        CU(cudaEventCreate(&r.b));
-        CU(cudaEventRecord(r.a, h->stream));
-    }
-    CU(launch_pass(P, h->num_sms, h->stream));
-    ++h->launches;
-    if (h->profiling) {
-        CU(cudaEventRecord(r.b, h->stream));
-        h->prof.push_back(r);
-    }
-    return SPEC_OK;
-}
-
 void free_all(spec_model* h) {
     for (auto& kv : h->graphs) cudaGraphExecDestroy(kv.second.exec);
     h->graphs.clear();
@@ -903,11 +719,9 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     }
     h->num_sms = prop.multiProcessorCount;
     if (const char* e = std::getenv("SPEC_NO_PDL")) h->pdl = !(e[0] == '1');
-    if (const char* e = std::getenv("SPEC_PASS_KERNEL")) h->use_pass = (e[0] == '1');
     if (const char* e = std::getenv("SPEC_GRAPHS")) h->use_graphs = !(e[0] == '0');
     TRYCU(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
     TRYCU(gemm_configure(h->device));
-    TRYCU(pass_configure(h->device));
     TRYCU(attention_configure(h->device));
 
     const int d = c.d_model, hd = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads;
@@ -1002,7 +816,6 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     TRY(dalloc_t(h, &h->ss, (size_t)kMaxBlock * (d / kTileRows)));
     TRY(dalloc_t(h, &h->attn_o, (size_t)Hkv * 2 * h->nch * 64 * hd));
     TRY(dalloc_t(h, &h->attn_ml, (size_t)Hkv * 2 * h->nch * 64));
-    TRY(dalloc_t(h, &h->gbar, 2));
     TRY(dalloc_t(h, &h->gpart, (size_t)2 * h->num_sms * kTileRows * kMaxBlock));
     TRY(dalloc_t(h, &h->gcnt, (size_t)h->max_T + 1));
     TRY(dalloc_t(h, &h->amax_val, (size_t)kMaxBlock * h->lm.T));
@@ -1039,12 +852,6 @@ spec_status spec_set_draft_plan(spec_handle h, const int32_t* draft_layers, int3
     if (s != SPEC_OK) return s;
     CU(cudaStreamSynchronize(h->stream));
     clear_graphs(h);
-    for (auto it = h->tables.begin(); it != h->tables.end();) {
-        if (it->first / 10000 == 1)
-            it = h->tables.erase(it);   // draft tables point at the old draft pools
-        else
-            ++it;
-    }
     if ((s = alloc_draft(h, draft_layers, n_draft_layers)) != SPEC_OK) return s;
     h->launches = 0;
     CU(launch_rollback(h->st, 1, 0, h->stream, false));
@@ -1153,12 +960,6 @@ spec_status spec_share_prefix(spec_handle h, int32_t enable) {
     if (h->plan_draft.empty()) return fail(SPEC_ERR_STATE, "model has no draft plan");
     CU(cudaStreamSynchronize(h->stream));
     clear_graphs(h);
-    for (auto it = h->tables.begin(); it != h->tables.end();) {
-        if (it->first / 10000 == 1)
-            it = h->tables.erase(it);   // draft tables point at the old draft pools
-        else
-            ++it;
-    }
     h->share_prefix = enable != 0;
     const std::vector<int32_t> plan = h->plan_draft;
     spec_status s = alloc_draft(h, plan.data(), (int32_t)plan.size());
@@ -1360,7 +1161,6 @@ spec_status spec_check_error(spec_handle h) {
         int zero = 0;
         CU(cudaMemcpy(&h->st->error, &zero, sizeof(int), cudaMemcpyHostToDevice));
         CU(cudaMemset(h->gcnt, 0, sizeof(int) * (h->max_T + 1)));
-        CU(cudaMemset(h->gbar, 0, sizeof(int) * 2));
         return fail(err == 10 ? SPEC_ERR_INVALID_ARG : SPEC_ERR_TIMEOUT,
                     err == 10 ? "a token id outside [0, vocab) was replaced by 0" : "device error code %d", err);
     }
@@ -1457,17 +1257,8 @@ spec_status spec_trace_enable(spec_handle h, int32_t enable) {
 
 spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int32_t* nphase, int32_t* nctas) {
     if (!h || !out || !nphase || !nctas) return fail(SPEC_ERR_INVALID_ARG, "null argument");
-    if (!h->trace || h->trace_mode == 0) return fail(SPEC_ERR_STATE, "no traced pass");
+    if (!h->trace || !h->tracing) return fail(SPEC_ERR_STATE, "no traced pass");
     CU(cudaStreamSynchronize(h->stream));
-    if (h->trace_mode == 1) {
-        if (h->trace_nphase == 0) return fail(SPEC_ERR_STATE, "no traced pass");
-        const size_t count = (size_t)h->num_sms * h->trace_nphase * 4;
-        if ((size_t)capacity < count) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", count);
-        CU(cudaMemcpy(out, h->trace, count * sizeof(long long), cudaMemcpyDeviceToHost));
-        *nphase = h->trace_nphase;
-        *nctas = h->num_sms;
-        return SPEC_OK;
-    }
     // separate launches: device layout [launch][kTraceCtas][4] -> [kTraceCtas][launch][4]
     const size_t nl = h->trace_kinds.size();
     if (nl == 0) return fail(SPEC_ERR_STATE, "no traced pass");
@@ -1485,7 +1276,7 @@ spec_status spec_trace_read(spec_handle h, long long* out, int32_t capacity, int
 
 spec_status spec_trace_kinds(spec_handle h, int32_t* out, int32_t capacity, int32_t* count) {
     if (!h || !out || !count) return fail(SPEC_ERR_INVALID_ARG, "null argument");
-    if (!h->trace || h->trace_mode == 0) return fail(SPEC_ERR_STATE, "no traced pass");
+    if (!h->trace || !h->tracing) return fail(SPEC_ERR_STATE, "no traced pass");
     const size_t nl = h->trace_kinds.size();
     if ((size_t)capacity < nl) return fail(SPEC_ERR_INVALID_ARG, "need %zu entries", nl);
     for (size_t i = 0; i < nl; ++i) out[i] = h->trace_kinds[i];

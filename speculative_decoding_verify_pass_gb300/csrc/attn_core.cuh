@@ -1,5 +1,4 @@
-// Attention building blocks shared by the standalone attention kernels and
-// the persistent pass kernel.
+// Attention building blocks of the attention kernels (attention.cu).
 //
 // A unit is (kv head h, 128-position chunk c); its 8 warps split each group
 // of 16 query rows by keys for S = Q K^T and by output dimensions for O = P V

@@ -1,6 +1,5 @@
-// Core of the weight-streaming GEMM shared by the per-kernel launcher
-// (gemm.cu) and the persistent pass kernel (pass.cu): stage ring layout,
-// stream-K / work-item iterators, expert work lists and the fused epilogues.
+// Core of the weight-streaming GEMM (gemm.cu): stage ring layout, stream-K /
+// work-item iterators, expert work lists and the fused epilogues.
 #pragma once
 
 #include <math.h>
@@ -620,22 +619,6 @@ __device__ __forceinline__ void convert_stage(uint8_t* xs, const float* rstd_op,
             *reinterpret_cast<uint2*>(xs + (t * 32 + lane) * 8) =
                 make_uint2(pack_bf16x2(v[t].x * r, v[t].y * r), pack_bf16x2(v[t].z * r, v[t].w * r));
         }
-    }
-}
-
-// Runtime dispatch of the epilogue kinds (the persistent pass kernel runs
-// every kind from one kernel).
-__device__ __forceinline__ void epilogue_any(int epi, const GemmParams& p, GemmSmem& sm, int tile, int item, int tid) {
-    switch (epi) {
-        case EPI_QKV: epilogue<EPI_QKV>(p, sm, tile, item, tid); break;
-        case EPI_RESID: epilogue<EPI_RESID>(p, sm, tile, item, tid); break;
-        case EPI_SWIGLU: epilogue<EPI_SWIGLU>(p, sm, tile, item, tid); break;
-        case EPI_LMHEAD: epilogue<EPI_LMHEAD>(p, sm, tile, item, tid); break;
-        case EPI_ROUTER: epilogue<EPI_ROUTER>(p, sm, tile, item, tid); break;
-        case EPI_EXPERT_SWIGLU: epilogue<EPI_EXPERT_SWIGLU>(p, sm, tile, item, tid); break;
-        case EPI_EXPERT_DOWN: epilogue<EPI_EXPERT_DOWN>(p, sm, tile, item, tid); break;
-        case EPI_STORE: epilogue<EPI_STORE>(p, sm, tile, item, tid); break;
-        default: break;
     }
 }
 

@@ -210,44 +210,6 @@ cudaError_t launch_pack(const PackSrc& s, const PackedMat& m, cudaStream_t st);
 cudaError_t launch_kv_io(uint16_t* pool, const int* block_table, uint16_t* logical, int ctx, int hkv, int hd,
                          bool to_pool, cudaStream_t s);
 
-// ---------------------------------------------------------------------------
-// Persistent pass kernel: one cooperative launch runs a whole pass as a list
-// of phases separated by grid barriers; weight stages of later phases stream
-// through the shared TMA ring while earlier phases finish.
-enum PhaseKind : int { PH_EMBED = 0, PH_GEMM = 1, PH_ATTN = 2, PH_COMB = 3, PH_ACCEPT = 4, PH_ADVANCE = 5 };
-
-struct PhaseDesc {
-    int kind;
-    GemmParams g;    // PH_GEMM (dense stream-K; the LM head too)
-    AttnParams a;    // PH_ATTN / PH_COMB (part_o / part_ml indexed by 64-position page)
-    EmbedParams e;   // PH_EMBED
-};
-
-struct PassParams {
-    const PhaseDesc* phases;   // device array
-    int nphase;
-    int n, which, mode;        // mode: AcceptMode for the final PH_ACCEPT
-    int nch;                   // 128-position chunks the KV pages cover
-    DevState* st;
-    int* gbar;                 // [2]: phase arrivals, finished CTAs (zero between launches)
-    // per-call buffers patched into the phases
-    const int* tokens;
-    float* logits;
-    const int* block;
-    int* out_argmax;
-    int* out_accept;
-    int* out_pair;
-    int* out_token;
-    const float* amax_val;
-    const int* amax_idx;
-    int lm_T;
-    long long* trace;          // optional [grid][nphase][3] globaltimer stamps (start, waited, done)
-};
-
-cudaError_t pass_configure(int device);
-cudaError_t launch_pass(const PassParams& p, int grid, cudaStream_t s);
-size_t pass_smem_bytes();
-
 // Sets the thread-local message returned by spec_last_error (api.cu).
 void set_last_error(const char* msg);
 

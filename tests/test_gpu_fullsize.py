@@ -53,12 +53,9 @@ def _load_context(m, cfg, ctx):
 
 
 @pytest.mark.parametrize("case", DENSE)
-def test_dense_fullsize_verify_matches_oracle(case, monkeypatch):
-    """The default launch path; the n=6 case runs the persistent pass kernel."""
+def test_dense_fullsize_verify_matches_oracle(case):
     torch = torch_cuda()
     c = FLOOR[case]
-    if case.endswith("-n6"):
-        monkeypatch.setenv("SPEC_PASS_KERNEL", "1")
     cfg = _config(c)
     w = synth.make_weights(cfg)
     m = make_model(cfg, w)

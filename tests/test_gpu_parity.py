@@ -299,11 +299,11 @@ def test_argument_errors(torch, tiny_cfg, tiny_model):
     m.check_error()
 
 
-@pytest.mark.parametrize("use_pass", ["0", "1"])
-def test_both_launch_paths_match_oracle(torch, tiny_cfg, tiny_oracle, tiny_prompt, monkeypatch, use_pass):
-    """Dense models run either as one persistent pass kernel (default) or as
-    one launch per phase; both must match the oracle and the golden greedy."""
-    monkeypatch.setenv("SPEC_PASS_KERNEL", use_pass)
+@pytest.mark.parametrize("graphs", ["1", "0"])
+def test_both_launch_paths_match_oracle(torch, tiny_cfg, tiny_oracle, tiny_prompt, monkeypatch, graphs):
+    """Passes run either from captured CUDA graphs (default) or as direct
+    launches (SPEC_GRAPHS=0); both must match the oracle and the golden greedy."""
+    monkeypatch.setenv("SPEC_GRAPHS", graphs)
     w = tiny_model_weights(tiny_cfg)
     m = make_model(tiny_cfg, w, draft_plan=oracle.layer_skip_plan(tiny_cfg.n_layers, 0.5))
     orc = tiny_oracle
@@ -314,7 +314,7 @@ def test_both_launch_paths_match_oracle(torch, tiny_cfg, tiny_oracle, tiny_promp
     for n in (1, 7, 16):
         am, acc, lg, _ = m.verify(torch.tensor(p[90:90 + n], dtype=torch.int32, device="cuda"), logits=True)
         ref, _, _ = orc.forward(oc, orc.full_plan, p[90:90 + n], 90)
-        assert_logits_close(lg.cpu().numpy(), ref, "path %s n=%d" % (use_pass, n))
+        assert_logits_close(lg.cpu().numpy(), ref, "graphs %s n=%d" % (graphs, n))
         argmax_mismatches(am.cpu().numpy(), ref)
         m.rollback(0, 90)
         oc.truncate(90)
