@@ -1497,7 +1497,10 @@ def trace_breakdown(stamps, kinds):
         ready = int(rd.min()) if len(rd) else int(live[:, 0].min())
         wk = live[live[:, 2] > 0, 2]
         ex = int(live[:, 3].max())
-        e = out.setdefault(TRACE_KIND_NAMES.get(int(kind), str(int(kind))),
+        name = TRACE_KIND_NAMES.get(int(kind), str(int(kind)))
+        if int(kind) == 1 and l > 0:     # a residual GEMM after the attention merge is the O projection
+            name = {17: "o_proj", 2: "down"}.get(int(kinds[l - 1]), name)
+        e = out.setdefault(name,
                            {"launches": 0, "ready_to_exit": 0.0, "work_to_exit": 0.0, "gap": 0.0, "gaps": 0,
                             "ready_spread": 0.0, "cta_ready_to_work_med": 0.0, "cta_ready_to_work_max": 0.0,
                             "work_spread": 0.0})

@@ -100,7 +100,7 @@ struct spec_model {
     int bat_nseq = 0;                   // > 0 while a batched pass is built
     PackedMat ctx_fc;                   // block-draft conditioning: fc [d][ctx_n_in*d]
     int ctx_n_in = 0;
-    uint8_t* xf_ctx = nullptr;          // its operand: the concatenated taps, fp32 fragment order
+    uint8_t* xf_ctx = nullptr;          // its operand: the concatenated taps, fp32 (xfrag32_offset order)
     std::vector<int> tap_of_layer;      // hidden-state taps: slot of each layer in tap_out, or -1
     float* tap_out = nullptr;           // caller's [count][16][d_model] fp32 buffer
     int tap_count = 0;
@@ -531,6 +531,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         a.n_kv_heads = c.n_kv_heads;
         a.head_dim = hd;
         a.nch = h->nch;
+        a.num_sms = h->num_sms;
         a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
         a.trace = trace_slot(h, kTraceAttnPartial, 2);
         CU(launch_attention(a, h->stream, pdl));

@@ -43,25 +43,20 @@ __device__ __forceinline__ uint16_t f2bf(float f) {
 __device__ __forceinline__ float bf_round(float f) { return bf2f(f2bf(f)); }
 
 // Byte offset of activation element (row j, k) inside one 64-wide k-block of
-// the fragment-ordered operand layout: [n8 tile][k16][lane][b0b1, b2b3].
-// This is exactly the order in which mma.m16n8k16's B fragments are read,
-// so the streaming GEMM loads each fragment with one 8-byte shared load.
+// a bf16 GEMM operand: the tensor core's canonical K-major layout without
+// swizzle, [8-row group][8-k group][row][8 k] -- "core matrices" of 8 rows x
+// 16 bytes, 128 bytes each, the next core matrix along k 128 bytes further
+// and the next 8-row group 1024 bytes further.  The streaming GEMM's MMA reads
+// a stage of this layout straight from shared memory.
 __device__ __forceinline__ int xfrag_offset(int j, int kk) {
-    const int n8 = j >> 3, g = j & 7;
-    const int k16 = kk >> 4, kin = kk & 15;
-    const int half = kin >> 3, c = (kin & 7) >> 1, e = kin & 1;
-    const int lane = g * 4 + c;
-    return (((n8 * 4 + k16) * 32 + lane) * 8) + half * 4 + e * 2;
+    return ((((j >> 3) * 8 + (kk >> 3)) * 8 + (j & 7)) * 16) + (kk & 7) * 2;
 }
 
-// fp32 variant for operands that a normalisation scales before rounding:
-// [n8 tile][k16][lane][b0, b1, b2, b3 as floats], 16 bytes per lane.
+// fp32 variant for operands that a normalisation scales before rounding: the
+// same order with 32-byte units (8 floats of one row), so that the GEMM's
+// converter turns unit u of 32 bytes into unit u of 16 bytes in place.
 __device__ __forceinline__ int xfrag32_offset(int j, int kk) {
-    const int n8 = j >> 3, g = j & 7;
-    const int k16 = kk >> 4, kin = kk & 15;
-    const int half = kin >> 3, c = (kin & 7) >> 1, e = kin & 1;
-    const int lane = g * 4 + c;
-    return (((n8 * 4 + k16) * 32 + lane) * 16) + (half * 2 + e) * 4;
+    return ((((j >> 3) * 8 + (kk >> 3)) * 8 + (j & 7)) * 32) + (kk & 7) * 4;
 }
 
 // Bytes of one operand stage (n rows, bf16 or fp32) and one k-block's stride.
@@ -181,6 +176,111 @@ __device__ __forceinline__ void cp_async_wait_all() {
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------- tcgen05 (sm_100+) ---
+// The fifth-generation tensor core: one thread issues an MMA whose operands
+// come from shared memory through matrix descriptors and whose fp32
+// accumulator lives in tensor memory (TMEM, 128 lanes x 512 columns of 32 bit
+// per SM); warps read the accumulator back with tcgen05.ld.
+
+// Allocate `ncols` TMEM columns (a power of two >= 32); the base address is
+// written to shared memory.  One whole warp executes it.
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(smem_dst)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Order tcgen05 operations around thread synchronisation (barriers, mbarrier waits).
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Make this thread's ordinary shared-memory writes visible to the tensor core
+// (the async proxy) before an MMA reads them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major, unswizzled operand in the
+// layout of xfrag_offset: core matrices 128 bytes apart along k (leading
+// byte offset) and 1024 bytes apart per 8-row group (stride byte offset);
+// bits 46..48 hold the fixed value 0b001.  Adding 16 advances the start
+// address by 256 bytes, one k16 step.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both
+// operands K-major, M = 128 (bits 24..28: M >> 4), N = 16 (bits 17..22: N >> 3).
+constexpr uint32_t kUmmaIdescM128N16 = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+
+// D[tmem] (+)= A[128 x 16] * B[16 x 16]^T; accumulate = 0 starts from zero.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kUmmaIdescM128N16), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on an mbarrier when every MMA this thread issued so far has
+// completed, i.e. its shared-memory operands may be overwritten and its
+// accumulator read.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+// 8 consecutive fp32 columns at each of G TMEM addresses of this warp's 32
+// lanes (lane i of the warp reads TMEM lane (warp % 4) * 32 + i), then one
+// wait for all G loads.
+__device__ __forceinline__ void tmem_ld8x2(uint32_t t0, uint32_t t1, float (&v)[2][8]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%16];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%17];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(t0), "r"(t1)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i >> 3][i & 7] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld8x4(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, float (&v)[4][8]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i >> 3][i & 7] = __uint_as_float(r[i]);
+}
+
+// 8 consecutive fp32 columns of this warp's 32 TMEM lanes (lane i of the
+// warp reads TMEM lane (warp % 4) * 32 + i), waiting for the load.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 // D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -188,6 +288,19 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Four (x4) or two (x2) 8x8 b16 matrices from shared memory: lanes 8i..8i+7
+// give the row addresses of matrix i (16 contiguous bytes each); register i
+// receives matrix i in the mma fragment distribution (lane 4g+c holds row g,
+// columns 2c, 2c+1).
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
 }
 
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {

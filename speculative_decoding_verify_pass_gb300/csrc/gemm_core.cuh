@@ -12,7 +12,14 @@ namespace gemm_core {
 constexpr int kStages = 10;  // 160 KB of weights in flight per SM
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 64;  // + one producer warp + one operand-converter warp
+constexpr int kConverterWarps = 2;   // convert alternate fp32 operand stages
+constexpr int kThreads = kConsumers + 64 + 32 * kConverterWarps;  // + producer, MMA issuer, converters
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kIssuerWarp = kConsumerWarps + 1;
+constexpr int kConverterWarp0 = kConsumerWarps + 2;
+constexpr int kReadGroup = 4;        // stage accumulators a consumer warp reads per wait
+constexpr int kAccCols = 16;   // TMEM columns of one stage's accumulator (N = 16 token columns)
+constexpr uint32_t kTmemCols = 256;   // power of two >= kStages * kAccCols
 constexpr int kCsLd = 20;  // padded row stride of the fp32 tile
 constexpr int kMaxItems = kMaxBlock * kMaxTopK + kMaxShared;
 constexpr int kPartFloats = kTileRows * kMaxBlock;
@@ -28,9 +35,12 @@ struct __align__(128) GemmSmem {
     uint8_t w[kStages][kStageWBytes];
     uint8_t x[kStages][kStageX32Bytes];
     float cs[kTileRows * kCsLd];
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    uint64_t ready[kStages];   // fp32 operand stage converted to bf16 fragments in place
+    uint64_t full[kStages];    // weights and operand of the stage have landed (bulk copies)
+    uint64_t ready[kStages];   // fp32 operand stage converted to bf16 in place (normalised operands)
+    uint64_t mdone[kStages];   // the stage's MMAs completed: its shared memory is free, its accumulator readable
+    uint64_t tfree[kStages];   // every consumer warp has read the stage's accumulator
+    uint64_t empty[kStages];   // mma.sync path: every consumer warp is done with the stage
+    uint32_t tmem_base;        // TMEM address of the accumulator ring (kStages x kAccCols columns)
     float rstd[kMaxBlock];     // applied in the epilogue (bf16 operands)
     float rstd_op[kMaxBlock];  // applied to fp32 operands before rounding
     int slots[kMaxContrib];
@@ -381,25 +391,40 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
 
 
 
-// Accumulators of one tile segment -> shared fp32 tile; for a tile split
-// between CTAs (stream-K), the other contributors publish their partials and
-// the first contributor sums all partials in contributor order.  Returns true when this CTA holds
-// the complete tile (and must run the epilogue), false otherwise.
-__device__ __forceinline__ bool finish_tile(const GemmParams& p, GemmSmem& sm, int tile, int b0, int b1,
-                                            const float (&acc0)[4], const float (&acc1)[4], int tid) {
+// Accumulators of one tile segment -> the shared fp32 tile cs[row][token].
+// tcgen05 consumers: thread (warp w, lane l) holds weight row 32*(w%4) + l,
+// token columns 8*(w/4) .. +7 (its TMEM lane and columns).
+__device__ __forceinline__ void store_acc_tc(GemmSmem& sm, const float (&acc)[8], int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    float* crow = sm.cs + (32 * (warp & 3) + lane) * kCsLd + 8 * (warp >> 2);
+    *reinterpret_cast<float4*>(crow) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(crow + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+// mma.sync consumers: warp w holds rows 16w..16w+15 in the m16n8 accumulator
+// distribution, acc0 for tokens 0..7 and acc1 for tokens 8..15.
+__device__ __forceinline__ void store_acc_mma(GemmSmem& sm, const float (&acc0)[4], const float (&acc1)[4], int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
+    float* cs = sm.cs;
+    const int r0 = warp * 16 + g;
+    cs[r0 * kCsLd + 2 * c] = acc0[0];
+    cs[r0 * kCsLd + 2 * c + 1] = acc0[1];
+    cs[(r0 + 8) * kCsLd + 2 * c] = acc0[2];
+    cs[(r0 + 8) * kCsLd + 2 * c + 1] = acc0[3];
+    cs[r0 * kCsLd + 8 + 2 * c] = acc1[0];
+    cs[r0 * kCsLd + 8 + 2 * c + 1] = acc1[1];
+    cs[(r0 + 8) * kCsLd + 8 + 2 * c] = acc1[2];
+    cs[(r0 + 8) * kCsLd + 8 + 2 * c + 1] = acc1[3];
+}
+
+// After the accumulators are in cs: for a tile split between CTAs
+// (stream-K), the other contributors publish their partials and the first
+// contributor sums all partials in contributor order.  Returns true when
+// this CTA holds the complete tile (and must run the epilogue), false
+// otherwise.
+__device__ __forceinline__ bool finish_tile(const GemmParams& p, GemmSmem& sm, int tile, int b0, int b1, int tid) {
     const long long I = (long long)p.T * p.KBs;
         float* cs = sm.cs;
-        const int r0 = warp * 16 + g;
-        cs[r0 * kCsLd + 2 * c] = acc0[0];
-        cs[r0 * kCsLd + 2 * c + 1] = acc0[1];
-        cs[(r0 + 8) * kCsLd + 2 * c] = acc0[2];
-        cs[(r0 + 8) * kCsLd + 2 * c + 1] = acc0[3];
-        cs[r0 * kCsLd + 8 + 2 * c] = acc1[0];
-        cs[r0 * kCsLd + 8 + 2 * c + 1] = acc1[1];
-        cs[(r0 + 8) * kCsLd + 8 + 2 * c] = acc1[2];
-        cs[(r0 + 8) * kCsLd + 8 + 2 * c + 1] = acc1[3];
         named_bar_sync(1, kConsumers);
 
         if (!p.items_mode && !(b0 == 0 && b1 == p.KBs)) {
@@ -508,62 +533,15 @@ __device__ __forceinline__ void compute_rstd(const GemmParams& p, GemmSmem& sm, 
     named_bar_sync(1, kConsumers);
 }
 
-// One ring stage of the MMA main loop: warp `warp` multiplies its 16 weight
-// rows by the stage's operand (one or two n8 token tiles).  fp32 operands are
-// scaled by rstd and rounded to bf16 here, which is where the normalisation's
-// rounding happens.
-//
-// The four k16 products of a stage start from zero and the stage sum is added
-// to the running accumulator with an ordinary round-to-nearest fp32 add.  The
-// tensor core's own accumulation does not round to nearest; chaining every k16
-// step into the running sum applies its rounding at the magnitude of the whole
-// dot product once per 16 terms.  On a one-layer model of width 2560 that put
-// the logits about 5x further from fp64-accumulated results than this split.
-__device__ __forceinline__ void mma_stage(const GemmSmem& sm, int s, int warp, int lane, bool two, bool f32,
-                                          float ra0, float ra1, float (&run0)[4], float (&run1)[4]) {
-    const uint8_t* ws = sm.w[s] + warp * 2048 + lane * 16;
-    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-    if (f32) {
-        const uint8_t* xs = sm.x[s] + lane * 16;
-#pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16) {
-            const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
-            const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-            const float4 v = *reinterpret_cast<const float4*>(xs + k16 * 512);
-            mma_bf16_16816(acc0, a, pack_bf16x2(v.x * ra0, v.y * ra0), pack_bf16x2(v.z * ra0, v.w * ra0));
-            if (two) {
-                const float4 w = *reinterpret_cast<const float4*>(xs + 2048 + k16 * 512);
-                mma_bf16_16816(acc1, a, pack_bf16x2(w.x * ra1, w.y * ra1), pack_bf16x2(w.z * ra1, w.w * ra1));
-            }
-        }
-    } else {
-        const uint8_t* xs = sm.x[s] + lane * 8;
-#pragma unroll
-        for (int k16 = 0; k16 < 4; ++k16) {
-            const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
-            const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-            const uint2 bv = *reinterpret_cast<const uint2*>(xs + k16 * 256);
-            mma_bf16_16816(acc0, a, bv.x, bv.y);
-            if (two) {
-                const uint2 bw = *reinterpret_cast<const uint2*>(xs + 1024 + k16 * 256);
-                mma_bf16_16816(acc1, a, bw.x, bw.y);
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        run0[i] += acc0[i];
-        run1[i] += acc1[i];
-    }
-}
-
-// P ring stages (bf16 operands) at once: the stages' MMA chains are
-// independent, so issuing them interleaved hides the tensor-core latency that
-// a single four-deep chain exposes.  TWO (n > 8: a second n8 token tile) is a
-// compile-time choice: a run-time branch around the MMAs inside this loop
-// costs about three times the loop's own time.  The arithmetic is exactly mma_stage's,
-// stage by stage: every stage's four k16 products start from zero, and the
-// stage sums are added to the running accumulator in stage order.
+// P ring stages at once on the mma.sync path, fragments loaded with
+// ldmatrix from the canonical layout (weights and operand alike: a core
+// matrix of 8 rows x 16 bytes is one 8x8 b16 matrix).  Warp `warp` owns weight
+// rows 16*warp..+15; per k16 step its A fragment is the core matrices (row
+// groups 2w, 2w+1) x (k groups 2k16, 2k16+1), its B fragment the token
+// group(s) x the same k groups.  The stages' MMA chains are independent, so
+// issuing them interleaved hides the tensor-core latency of a single chain;
+// each stage's four k16 products start from zero, and the stage sums enter
+// the running accumulator in stage order (round-to-nearest adds).
 template <int P, bool TWO>
 __device__ __forceinline__ void mma_stages(const GemmSmem& sm, const int (&st)[4], int warp, int lane,
                                            float (&run0)[4], float (&run1)[4]) {
@@ -572,19 +550,26 @@ __device__ __forceinline__ void mma_stages(const GemmSmem& sm, const int (&st)[4
     for (int u = 0; u < P; ++u)
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc0[u][i] = acc1[u][i] = 0.f;
+    const int mi = lane >> 3, r = lane & 7;
+    // A: matrix mi = (row group 2w + (mi & 1), k group 2k16 + (mi >> 1))
+    const int a_off = ((2 * warp + (mi & 1)) * 8 + (mi >> 1)) * 128 + r * 16;
+    // B (x4 for two token groups): matrix mi = (token group mi >> 1, k group 2k16 + (mi & 1))
+    const int b_off = ((mi >> 1) * 8 + (mi & 1)) * 128 + r * 16;
 #pragma unroll
     for (int k16 = 0; k16 < 4; ++k16) {
 #pragma unroll
         for (int u = 0; u < P; ++u) {
-            const uint8_t* ws = sm.w[st[u]] + warp * 2048 + lane * 16;
-            const uint8_t* xs = sm.x[st[u]] + lane * 8;
-            const uint4 a4 = *reinterpret_cast<const uint4*>(ws + k16 * 512);
-            const uint32_t a[4] = {a4.x, a4.y, a4.z, a4.w};
-            const uint2 bv = *reinterpret_cast<const uint2*>(xs + k16 * 256);
-            mma_bf16_16816(acc0[u], a, bv.x, bv.y);
+            uint32_t a[4];
+            ldmatrix_x4(a, smem_u32(sm.w[st[u]]) + a_off + k16 * 256);
             if constexpr (TWO) {
-                const uint2 bw = *reinterpret_cast<const uint2*>(xs + 1024 + k16 * 256);
-                mma_bf16_16816(acc1[u], a, bw.x, bw.y);
+                uint32_t b[4];
+                ldmatrix_x4(b, smem_u32(sm.x[st[u]]) + b_off + k16 * 256);
+                mma_bf16_16816(acc0[u], a, b[0], b[1]);
+                mma_bf16_16816(acc1[u], a, b[2], b[3]);
+            } else {
+                uint32_t b[2];
+                ldmatrix_x2(b, smem_u32(sm.x[st[u]]) + (b_off & 255) + k16 * 256);
+                mma_bf16_16816(acc0[u], a, b[0], b[1]);
             }
         }
     }
@@ -597,28 +582,30 @@ __device__ __forceinline__ void mma_stages(const GemmSmem& sm, const int (&st)[4
         }
 }
 
-// Converts one ring stage's fp32 operand (x*gain, fp32 fragment order) in
-// place into bf16 B fragments of x*gain*rstd (the layout bf16 operands use),
-// by one warp: each lane reads its entries for every (n8, k16) first, then
-// writes, so the half-size output cannot overwrite unread input.  The
-// rounding is the one the consumers would otherwise do: fp32 product, then
-// bf16 round-to-nearest-even.
+// Converts one ring stage's fp32 operand (x*gain, xfrag32_offset order) in
+// place into the bf16 operand of x*gain*rstd (xfrag_offset order, the layout
+// the MMA reads), by one warp: unit u (8 values of one row) moves from bytes
+// 32u.. to 16u..; every lane reads all its units before any lane writes
+// (__syncwarp orders the reads before the other lanes' writes).  The rounding
+// is the normalisation's: fp32 product, then bf16 round-to-nearest-even.
 template <bool TWO>
 __device__ __forceinline__ void convert_stage(uint8_t* xs, const float* rstd_op, int lane) {
-    float4 v[8];
-    constexpr int entries = TWO ? 8 : 4;   // (n8, k16) pairs
+    constexpr int kUnits = TWO ? 4 : 2;   // 64 units (rows 0..7) or 128 (rows 0..15) per stage
+    float4 v[kUnits][2];
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
-        if (t < entries) v[t] = *reinterpret_cast<const float4*>(xs + (t * 32 + lane) * 16);
+    for (int t = 0; t < kUnits; ++t) {
+        const int u = lane + 32 * t;
+        v[t][0] = *reinterpret_cast<const float4*>(xs + u * 32);
+        v[t][1] = *reinterpret_cast<const float4*>(xs + u * 32 + 16);
+    }
     __syncwarp();
-    const float r0 = rstd_op[lane >> 2], r1 = rstd_op[8 + (lane >> 2)];
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        if (t < entries) {
-            const float r = t < 4 ? r0 : r1;
-            *reinterpret_cast<uint2*>(xs + (t * 32 + lane) * 8) =
-                make_uint2(pack_bf16x2(v[t].x * r, v[t].y * r), pack_bf16x2(v[t].z * r, v[t].w * r));
-        }
+    for (int t = 0; t < kUnits; ++t) {
+        const int u = lane + 32 * t;
+        const float r = rstd_op[((u >> 6) << 3) | (u & 7)];
+        *reinterpret_cast<uint4*>(xs + u * 16) =
+            make_uint4(pack_bf16x2(v[t][0].x * r, v[t][0].y * r), pack_bf16x2(v[t][0].z * r, v[t][0].w * r),
+                       pack_bf16x2(v[t][1].x * r, v[t][1].y * r), pack_bf16x2(v[t][1].z * r, v[t][1].w * r));
     }
 }
 

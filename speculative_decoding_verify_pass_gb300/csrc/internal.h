@@ -24,7 +24,7 @@ enum EpiKind : int {
 };
 
 // A weight matrix [N][K] repacked as tiles of 128 rows x 64 k in the order the
-// consumer warps read A fragments: [tile][kblock][m16 (8)][k16 (4)][lane][8 bf16].
+// tensor core reads them: [tile][kblock][8-row group (16)][8-k group (8)][row (8)][8 bf16].
 // Launch tracing: a traced launch gets kTraceCtas x 4 slots; CTA c writes
 // global-timer stamps at trace[c*4 + k]: k = 0 entry, 1 inputs ready (after
 // the dependency wait), 2 main work done, 3 exit (0 where a kernel has no such
@@ -114,6 +114,7 @@ struct AttnParams {
     uint8_t* xf_out;           // O-projection operand
     DevState* st;
     int which, n, n_heads, n_kv_heads, head_dim, nch;
+    int num_sms;               // the partial kernel's grid: about one CTA per SM
     float scale_log2;          // log2(e) / sqrt(hd)
     // batched sequences (seq_len != null): n rows per sequence, nseq of them;
     // sequence s: positions from seq_len[s], logical pages from s * seq_pages,
@@ -156,7 +157,7 @@ struct CombineParams {           // MoE: x += sum_s gate*y_slot[s] + sum_t y_slo
 cudaError_t launch_moe_combine(const CombineParams& p, cudaStream_t s, bool pdl);
 
 // Block-draft conditioning (context append): the tapped hidden states
-// [n_in][16][d] as one fp32 operand of K = n_in*d (fragment order, gain 1),
+// [n_in][16][d] as one fp32 operand of K = n_in*d (xfrag32_offset order, gain 1),
 // and fp32 rows [16][d] as a layer's normalised operand (x*gain + sum of
 // squares, as the embedding kernel writes them).
 struct ConcatParams {

@@ -24,7 +24,7 @@ cudaError_t launch_ex(const void* fn, dim3 grid, dim3 block, size_t smem, cudaSt
 }
 
 // Writes row j's 8 values starting at R0 into the residual, the next GEMM's
-// operand (x * gain, fp32, fragment order; the consumer applies rstd and
+// operand (x * gain, fp32, xfrag32_offset order; the consumer applies rstd and
 // rounds) and returns their sum of squares.
 __device__ __forceinline__ float store_residual8(float* xr, const float (&v)[8], int j, int R0, const uint16_t* g_next,
                                                  uint8_t* xf_out) {
@@ -273,20 +273,21 @@ __device__ __forceinline__ uint16_t pack_fetch(const PackSrc& s, int N, int r, i
     return 0;
 }
 
-// One thread per 16-byte A fragment chunk of the packed layout.
+// One thread per 16-byte chunk (8 consecutive k of one row) of the packed
+// layout: a stage is [8-row group (16)][8-k group (8)][row (8)][8 k], the
+// tensor core's canonical K-major layout (see xfrag_offset).
 __global__ void pack_kernel(PackSrc s, uint8_t* out, int N, int T, int KBs) {
     const long long total = (long long)T * KBs * (kStageWBytes / 16);
     for (long long ch = blockIdx.x * (long long)blockDim.x + threadIdx.x; ch < total;
          ch += (long long)gridDim.x * blockDim.x) {
-        const int lane = (int)(ch & 31), k16 = (int)((ch >> 5) & 3), m16 = (int)((ch >> 7) & 7);
+        const int r8 = (int)(ch & 7), k8 = (int)((ch >> 3) & 7), m8 = (int)((ch >> 6) & 15);
         const long long tb = ch >> 10;
         const int b = (int)(tb % KBs), t = (int)(tb / KBs);
-        const int g = lane >> 2, c = lane & 3;
-        const int r0 = t * kTileRows + m16 * 16 + g, r1 = r0 + 8;
-        const int k0 = b * kKBlock + k16 * 16 + 2 * c, k1 = k0 + 8;
-        uint16_t v[8] = {pack_fetch(s, N, r0, k0), pack_fetch(s, N, r0, k0 + 1), pack_fetch(s, N, r1, k0),
-                         pack_fetch(s, N, r1, k0 + 1), pack_fetch(s, N, r0, k1), pack_fetch(s, N, r0, k1 + 1),
-                         pack_fetch(s, N, r1, k1), pack_fetch(s, N, r1, k1 + 1)};
+        const int r = t * kTileRows + m8 * 8 + r8;
+        const int k0 = b * kKBlock + k8 * 8;
+        uint16_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = pack_fetch(s, N, r, k0 + e);
         *reinterpret_cast<uint4*>(out + ch * 16) = *reinterpret_cast<const uint4*>(v);
     }
 }
