@@ -359,6 +359,15 @@ double expert_launch_bytes(spec_model* h, const GemmParams& p, int layer) {
     return items * per + (double)n * p.KBs * kKBlock * 2.0;
 }
 
+// Chunk groups of the attention partials: about the SMs per kv head (one
+// wave of partial CTAs for a single sequence), at most the chunks a cache
+// holds.  Fixed per model, so every pass groups a position's chunk alike.
+int attn_groups(const spec_model* h) {
+    int g = (h->num_sms + h->c.n_kv_heads - 1) / h->c.n_kv_heads;
+    if (g < 1) g = 1;
+    return g < h->nch ? g : h->nch;
+}
+
 // Next launch slot of a traced pass (nullptr when not tracing or full).
 long long* trace_slot(spec_model* h, int kind, int slots = 1) {
     if (!h->trace || !h->tracing) return nullptr;
@@ -532,6 +541,7 @@ spec_status run_pass_launch(spec_model* h, int which, const int32_t* d_tokens, i
         a.head_dim = hd;
         a.nch = h->nch;
         a.num_sms = h->num_sms;
+        a.groups = attn_groups(h);
         a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
         a.trace = trace_slot(h, kTraceAttnPartial, 2);
         CU(launch_attention(a, h->stream, pdl));

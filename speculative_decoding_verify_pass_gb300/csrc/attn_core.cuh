@@ -3,9 +3,11 @@
 // A unit is (kv head h, 128-position chunk c); its 8 warps split each group
 // of 16 query rows by keys for S = Q K^T and by output dimensions for O = P V
 // (bf16 tensor-core MMA, fp32 accumulation).  The unit writes one partial
-// (row max, row sum, unnormalised O) per row; partials are indexed by
-// absolute chunk, so a query's result never depends on the block size.  A
-// merge step combines the chunks of a row in increasing chunk order.
+// (row max, row sum, unnormalised O) per row into the slot of its chunk's
+// group (chunk mod S, S fixed per model), merging it into the chunks of the
+// group that came before; the grouping depends only on absolute positions,
+// so a query's result never depends on the block size.  A merge step
+// combines the groups of a row in increasing order.
 #pragma once
 
 #include <math.h>
@@ -27,6 +29,21 @@ constexpr int kAttnScratchBytes = 4 * kAttnSlotBytes;  // up to 4 row groups at 
 template <int HD>
 __host__ __device__ constexpr int q_stride() { return HD + 8; }
 
+// Merging two partials of one row, (m1, l1, O1) then (m2, l2, O2), maxima in
+// the log2 domain (-1e30 for a row with no key): with M = max(m1, m2), each
+// part is weighted by exp2(m - M).  A part with no key gets weight exactly
+// zero and the other weight exactly one, so merging an empty chunk changes
+// nothing.
+__device__ __forceinline__ float2 merge2(float2 o1, float m1, float2 o2, float m2) {
+    const float M = fmaxf(m1, m2);
+    const float w1 = exp2f(m1 - M), w2 = exp2f(m2 - M);
+    return make_float2(o1.x * w1 + o2.x * w2, o1.y * w1 + o2.y * w2);
+}
+__device__ __forceinline__ float2 merge_ml(float2 a, float2 b) {
+    const float M = fmaxf(a.x, b.x);
+    return make_float2(M, a.y * exp2f(a.x - M) + b.y * exp2f(b.x - M));
+}
+
 // One unit (kv head h, 128-position chunk) with all 8 warps.  sk0/sk1 and
 // sv0/sv1 are the K and V slabs of the chunk's two pages.
 //
@@ -46,13 +63,15 @@ __host__ __device__ constexpr int q_stride() { return HD + 8; }
 // So a row's result depends neither on the block size nor on C.  The unit
 // writes one partial (row max in the log2 domain, row sum, unnormalised O)
 // per row.  wait_slabs() is called once, after the first query fragments are
-// requested and before any slab is read.  qs, when given, holds the unit's
+// requested and before any slab is read.  The attention kernel picks C from
+// the number of row groups.  qs, when given, holds the unit's
 // query rows in shared memory ([R][HD+8]); otherwise they are read from
 // global memory.  scratch holds `slots` slot areas of kAttnSlotBytes.
 template <int HD, int C, class WaitSlabs>
 __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t* sk0, const uint16_t* sk1,
                                             const uint16_t* sv0, const uint16_t* sv1, float* scratch,
                                             const uint16_t* qs, int h, int chunk, int pos0, int n, size_t seq_base,
+                                            int group, bool accumulate, bool flush, float* run_o, float2* run_ml,
                                             int tid, WaitSlabs& wait_slabs) {
     constexpr int kTiles = HD / 16;                                   // dim tiles
     constexpr int par = 8 / C;                                        // row groups at once
@@ -68,7 +87,11 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
     float* ssum = smax + 128;                                         // [8][16]
     uint32_t* pf = reinterpret_cast<uint32_t*>(smax + 256);           // [8][32][8]
     const float k2 = a.scale_log2;
-    const size_t base = seq_base + ((size_t)h * a.nch + chunk) * 64;
+    // the partial of (kv head h, chunk group) runs in shared memory (run_o
+    // [row][HD], run_ml [row]): with `accumulate` it already holds the group's
+    // earlier chunks and this chunk is merged into it; with `flush` (the
+    // group's last chunk of this pass) it is then written to global memory
+    const size_t base = seq_base + ((size_t)h * a.nch + group) * 64;
     // barrier of the C warps sharing a slot (the whole CTA when C = 8)
     auto slot_sync = [&] {
         if (C == 8)
@@ -103,6 +126,13 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
         }
         const int limA = rA < R ? pos0 + rA / G : -1;
         const int limB = rB < R ? pos0 + rB / G : -1;
+        // the group's earlier maxima, read before any thread of the slot
+        // writes the merged ones (after the slot's next barrier)
+        float moA = -1e30f, moB = -1e30f;
+        if (accumulate && act) {
+            if (rA < R) moA = run_ml[rA].x;
+            if (rB < R) moB = run_ml[rB].x;
+        }
         float s[kgs][2][4];   // this warp's key groups
         if (act) {
 #pragma unroll
@@ -219,21 +249,35 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
                     mma_bf16_16816(oc[2 + pp][0], pl, r[0], r[1]);
                     mma_bf16_16816(oc[2 + pp][1], pl, r[2], r[3]);
                 }
+                // this thread owns the same elements of the running partial
+                // for every chunk, so it merges them without a barrier
                 if (rA < R) {
+                    float* run = run_o + rA * HD + tile * 16;
                     float* dst = a.part_o + (base + rA) * HD + tile * 16;
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
-                        *reinterpret_cast<float2*>(dst + t * 8 + 2 * cc) =
-                            make_float2((oc[0][t][0] + oc[1][t][0]) + (oc[2][t][0] + oc[3][t][0]),
-                                        (oc[0][t][1] + oc[1][t][1]) + (oc[2][t][1] + oc[3][t][1]));
+                    for (int t = 0; t < 2; ++t) {
+                        float2 v = make_float2((oc[0][t][0] + oc[1][t][0]) + (oc[2][t][0] + oc[3][t][0]),
+                                               (oc[0][t][1] + oc[1][t][1]) + (oc[2][t][1] + oc[3][t][1]));
+                        if (accumulate) v = merge2(*reinterpret_cast<const float2*>(run + t * 8 + 2 * cc), moA, v, msA);
+                        if (flush)
+                            *reinterpret_cast<float2*>(dst + t * 8 + 2 * cc) = v;
+                        else
+                            *reinterpret_cast<float2*>(run + t * 8 + 2 * cc) = v;
+                    }
                 }
                 if (rB < R) {
+                    float* run = run_o + rB * HD + tile * 16;
                     float* dst = a.part_o + (base + rB) * HD + tile * 16;
 #pragma unroll
-                    for (int t = 0; t < 2; ++t)
-                        *reinterpret_cast<float2*>(dst + t * 8 + 2 * cc) =
-                            make_float2((oc[0][t][2] + oc[1][t][2]) + (oc[2][t][2] + oc[3][t][2]),
-                                        (oc[0][t][3] + oc[1][t][3]) + (oc[2][t][3] + oc[3][t][3]));
+                    for (int t = 0; t < 2; ++t) {
+                        float2 v = make_float2((oc[0][t][2] + oc[1][t][2]) + (oc[2][t][2] + oc[3][t][2]),
+                                               (oc[0][t][3] + oc[1][t][3]) + (oc[2][t][3] + oc[3][t][3]));
+                        if (accumulate) v = merge2(*reinterpret_cast<const float2*>(run + t * 8 + 2 * cc), moB, v, msB);
+                        if (flush)
+                            *reinterpret_cast<float2*>(dst + t * 8 + 2 * cc) = v;
+                        else
+                            *reinterpret_cast<float2*>(run + t * 8 + 2 * cc) = v;
+                    }
                 }
             }
             if (sub == 0 && cc == 0) {
@@ -243,26 +287,22 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
                     LA += ssum[kg * 16 + g];
                     LB += ssum[kg * 16 + g + 8];
                 }
-                if (rA < R) a.part_ml[base + rA] = make_float2(msA, LA);
-                if (rB < R) a.part_ml[base + rB] = make_float2(msB, LB);
+                if (rA < R) {
+                    float2 ml = make_float2(msA, LA);
+                    if (accumulate) ml = merge_ml(run_ml[rA], ml);
+                    if (flush) a.part_ml[base + rA] = ml;
+                    else run_ml[rA] = ml;
+                }
+                if (rB < R) {
+                    float2 ml = make_float2(msB, LB);
+                    if (accumulate) ml = merge_ml(run_ml[rB], ml);
+                    if (flush) a.part_ml[base + rB] = ml;
+                    else run_ml[rB] = ml;
+                }
             }
         }
         if (rg0 + par < nrg) slot_sync();   // the slot's scratch is reused by the next round
     }
-}
-
-template <int HD, class WaitSlabs>
-__device__ __forceinline__ void attn_unit(const AttnParams& a, const uint16_t* sk0, const uint16_t* sk1,
-                                          const uint16_t* sv0, const uint16_t* sv1, float* scratch,
-                                          const uint16_t* qs, int slots, int h, int chunk, int pos0, int n,
-                                          size_t seq_base, int tid, WaitSlabs wait_slabs) {
-    const int nrg = (n * (a.n_heads / a.n_kv_heads) + 15) / 16;
-    if (slots <= 1 || nrg <= 1)
-        attn_unit_c<HD, 8>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, n, seq_base, tid, wait_slabs);
-    else if (nrg <= 2)
-        attn_unit_c<HD, 4>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, n, seq_base, tid, wait_slabs);
-    else
-        attn_unit_c<HD, 2>(a, sk0, sk1, sv0, sv1, scratch, qs, h, chunk, pos0, n, seq_base, tid, wait_slabs);
 }
 
 // Rows (query head, token) u0, u0+ustep, ...: one warp per row merges the nc
@@ -290,6 +330,7 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
             const int tot = a.seq_len[sq] + a.n;
             nc = (tot + kAttnChunk - 1) / kAttnChunk;
             if (nc > a.nch) nc = a.nch;
+            if (nc > a.groups) nc = a.groups;
         }
         const int h = qh / G, r = jl * G + qh % G;
         const size_t sbase = (size_t)sq * a.n_kv_heads * a.nch * 64;

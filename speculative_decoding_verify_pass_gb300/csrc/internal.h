@@ -115,6 +115,7 @@ struct AttnParams {
     DevState* st;
     int which, n, n_heads, n_kv_heads, head_dim, nch;
     int num_sms;               // the partial kernel's grid: about one CTA per SM
+    int groups;                // S: chunk c's partial is group c mod S's (fixed per model, <= nch)
     float scale_log2;          // log2(e) / sqrt(hd)
     // batched sequences (seq_len != null): n rows per sequence, nseq of them;
     // sequence s: positions from seq_len[s], logical pages from s * seq_pages,
