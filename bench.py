@@ -59,7 +59,11 @@ def measured_peaks():
 
 
 GEMM_SOURCES = ("common.cuh", "internal.h", "gemm_core.cuh", "gemm.cu")
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_kernel_dram_qwen3-4b.txt")
+
+
+def traffic_profile(model):
+    """The committed ncu capture of the streaming GEMM's DRAM bytes for a model shape."""
+    return os.path.join(ROOT, "profiles", "gemm_kernel_dram_%s.txt" % model)
 
 
 def gemm_source_sha256():
@@ -75,11 +79,14 @@ def gemm_source_sha256():
 def ncu_traffic(launches_by_kind, cfg, args):
     """DRAM bytes (read + write) per GEMM launch from the committed ncu
     capture, averaged over this run's launch mix by epilogue kind; None when
-    the capture is of another workload or of other GEMM sources."""
-    if not os.path.exists(TRAFFIC_PROFILE):
-        return None, "no ncu capture committed"
+    the capture is of another workload or of other GEMM sources.  The capture
+    may be of the model truncated to its first layers: the launches have the
+    same matrix shapes, so the same bytes per launch of each kind."""
+    path = traffic_profile(cfg.name)
+    if not os.path.exists(path):
+        return None, "no ncu capture committed for this model"
     per_kind, digest, model = {}, None, None
-    for line in open(TRAFFIC_PROFILE):
+    for line in open(path):
         f = line.split()
         if len(f) >= 2 and f[0] == "source_sha256":
             digest = f[1]
@@ -87,7 +94,7 @@ def ncu_traffic(launches_by_kind, cfg, args):
             model = f[1]
         elif len(f) == 6 and f[0] == "kind":
             per_kind[int(f[1])] = float(f[3]) + float(f[5])
-    if model != cfg.name or args.layers:
+    if model != cfg.name:
         return None, "ncu capture is of another model"
     if digest != gemm_source_sha256():
         return None, "GEMM sources changed since the ncu capture"
@@ -95,7 +102,7 @@ def ncu_traffic(launches_by_kind, cfg, args):
     if n == 0 or any(k not in per_kind for k, c in launches_by_kind.items() if c):
         return None, "ncu capture lacks a launch kind of this run"
     tot = sum(per_kind[k] * c for k, c in launches_by_kind.items() if c)
-    return round(tot / n), os.path.relpath(TRAFFIC_PROFILE, ROOT)
+    return round(tot / n), os.path.relpath(path, ROOT)
 
 
 def pass_bytes(cfg, n, ctx, plan=None):
@@ -322,7 +329,7 @@ def launch_segments(stamps, kinds):
 GEMM_KINDS = (0, 1, 2, 3)      # QKV, residual (O / down), SwiGLU gate-up, LM head
 
 
-def inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind, reps=3):
+def inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind, cfg, args, reps=3):
     """The streaming GEMM inside an unbracketed verify pass: algorithmic bytes
     per pass (from one event-profiled pass) over the GEMM launches' trace
     segments (launch_segments), averaged over `reps` traced passes."""
@@ -334,6 +341,7 @@ def inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind, reps=3):
     sv.spec_kv_rollback(m.h, 0, ctx)
     per_kind = {k: sv.spec_profile_read(m.h, k) for k in GEMM_KINDS}
     sv.spec_profile_enable(m.h, False)
+    traffic, traffic_note = ncu_traffic({k: v[2] for k, v in per_kind.items()}, cfg, args)
     gbytes = sum(v[1] for v in per_kind.values())
     glaunch = sum(v[2] for v in per_kind.values())
     sv.spec_trace_enable(m.h, True)
@@ -352,7 +360,7 @@ def inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind, reps=3):
     achieved = gbytes / (gus * 1e-6) / 1e9
     return {"kernel": "gemm_kernel (weight-streaming GEMM: QKV, O, gate-up, down, LM head)", "bound": "hbm",
             "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
             "timing": "global-timer launch trace of unbracketed verify passes: each launch owns the time from the "
                       "previous launch's last CTA exit to its own last CTA exit, so the GEMM segments plus the "
                       "other launches' segments add up to the traced pass",
@@ -480,7 +488,7 @@ def run_native_geometric(args):
 
     # ---- dominant kernel: the streaming GEMM inside unbracketed passes ----
     blk.copy_(d_blocks[0])
-    roof = inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind)
+    roof = inpipeline_gemm_roofline(m, torch, sv, blk, ctx, peak, peak_kind, cfg, args)
 
     # ---- end to end through the host-driven API (pinned copies each step) ----
     e2e = run_e2e_geometric(m, torch, sv, blocks, sched, ctx, args)

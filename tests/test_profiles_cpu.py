@@ -25,7 +25,7 @@ PROFILES = os.path.join(ROOT, "profiles")
 
 
 def _gemm_traffic():
-    path = os.path.join(PROFILES, "gemm_kernel_dram_qwen3-4b.txt")
+    path = os.path.join(PROFILES, "gemm_kernel_dram_llama-3.1-8b.txt")
     kinds = {}
     for line in open(path):
         f = line.split()
@@ -35,7 +35,7 @@ def _gemm_traffic():
 
 
 def test_dense_gemm_kinds_read_their_weights_once():
-    cfg = synth.qwen3_4b()
+    cfg = synth.llama31_8b()
     one_layer = closed_forms.pass_bytes(cfg, 1, 0, plan=[0])
     weights = {
         0: one_layer.qkv,
