@@ -96,3 +96,38 @@ def best_gamma(alpha: float, verify_time, draft_time: float, gammas) -> int:
         if best is None or rate > best_rate * (1.0 + 1e-12):
             best, best_rate = g, rate
     return best
+
+
+def fit_bandwidth(bytes_per_run, seconds_per_run):
+    """Effective bandwidth of one operation from repeated isolated runs of the
+    same bytes: the mean rate, and its relative spread (half the range of the
+    per-run rates over their mean), used as the bandwidth error."""
+    rates = [b / t for b, t in zip(bytes_per_run, seconds_per_run)]
+    mean = sum(rates) / len(rates)
+    return mean, (max(rates) - min(rates)) / (2.0 * mean)
+
+
+def dedup_saving(bytes_ps, bytes_dd, bw_ps: float, bw_dd: float, err_ps: float, err_dd: float):
+    """Time deduplication saves over per-slot reads on a pass whose expert
+    operations request bytes_ps[l] / bytes_dd[l] per layer l, at bandwidths
+    bw_ps / bw_dd with relative errors err_ps / err_dd.  A relative bandwidth
+    error e moves a time b/B by at most b/B * e/(1-e); the bound adds both
+    modes' moves.  Returns (saving, bound)."""
+    t_ps = sum(bytes_ps) / bw_ps
+    t_dd = sum(bytes_dd) / bw_dd
+    bound = t_ps * err_ps / (1.0 - err_ps) + t_dd * err_dd / (1.0 - err_dd)
+    return t_ps - t_dd, bound
+
+
+def predicted_verify_times(t_plain: float, expert_time, pass_sizes):
+    """Verify time per pass size from a plain one-token step's measured time
+    and the predicted expert time per pass size (bytes over fitted
+    bandwidth): the non-expert part is taken as the plain step's time less its
+    own predicted expert time, and held fixed."""
+    rest = t_plain - expert_time(1)
+    return {n: rest + expert_time(n) for n in pass_sizes}
+
+
+def gamma_staircase(alphas, verify_time, draft_time: float, gammas):
+    """Best draft length for each acceptance rate."""
+    return [best_gamma(float(a), verify_time, draft_time, gammas) for a in alphas]

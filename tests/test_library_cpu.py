@@ -111,3 +111,34 @@ def test_step_model_matches_oracle_closed_forms():
     assert abs(sm.alpha_for_mean_accept(9.0, 15) - 0.93293) < 1e-4
     moe = synth.moe_v2lite()
     assert sm.expert_bytes(moe) == 3 * 1408 * 2048 * 2
+
+
+def test_step_model_predictions_from_fitted_bandwidths():
+    """The MoE suite's prediction helpers: the saving and its bound, the
+    crossover they imply, and a monotone best-draft-length staircase from
+    predicted verify times."""
+    import numpy as np
+    from speculative_decoding_verify_pass_gb300 import stepmodel as sm
+    bw, err = sm.fit_bandwidth([10.0, 10.0, 10.0], [1.0, 1.25, 0.8])
+    assert abs(bw - (10.0 + 8.0 + 12.5) / 3) < 1e-12 and abs(err - 2.25 / bw) < 1e-12
+    # the saving equals the time identity, and the bound covers the saving
+    # under any bandwidths within the stated errors
+    bps, bdd = [3.0, 5.0], [2.0, 3.0]
+    s, bound = sm.dedup_saving(bps, bdd, 2.0, 1.5, 0.1, 0.05)
+    assert abs(s - (8.0 / 2.0 - 5.0 / 1.5)) < 1e-12
+    for f_ps in (0.9, 1.0, 1.1):
+        for f_dd in (0.95, 1.0, 1.05):
+            s2 = 8.0 / (2.0 * f_ps) - 5.0 / (1.5 * f_dd)
+            assert abs(s2 - s) <= bound + 1e-12
+    # crossover: the first pass size whose saving is positive is the first
+    # whose byte share is below the bandwidth ratio
+    ns = range(1, 9)
+    bw_ps, bw_dd = 1.0, 0.6
+    u = [1.0, 0.8, 0.7, 0.62, 0.55, 0.5, 0.47, 0.45]
+    sav = [sm.dedup_saving([1.0], [ui], bw_ps, bw_dd, 0.0, 0.0)[0] for ui in u]
+    assert sm.first_win(ns, u, [bw_dd / bw_ps] * 8) == next(n for n, v in zip(ns, sav) if v > 0) == 5
+    # predicted verify times: the plain step is reproduced; the staircase is monotone
+    tv = sm.predicted_verify_times(1000.0, lambda n: 200.0 + 40.0 * (n - 1), ns)
+    assert tv[1] == 1000.0 and tv[8] == 1000.0 + 280.0
+    st = sm.gamma_staircase(np.linspace(0.0, 1.0, 22), lambda n: tv[n], 300.0, range(0, 8))
+    assert st[0] == 0 and all(b >= a for a, b in zip(st, st[1:]))
