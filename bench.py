@@ -1270,11 +1270,40 @@ def suite_shared_prefix(args):
     m.close()
 
 
+def _expert_op_runs(torch, sv, m, toks, ctx, reps):
+    """Per run: (seconds, bytes requested) of the expert operation (gate-up
+    and down launches) of every MoE layer of one verify pass, each launch
+    bracketed by CUDA events, i.e. run alone."""
+    n = len(toks)
+    blk = torch.tensor(toks, dtype=torch.int32, device="cuda")
+    am = torch.zeros(n, dtype=torch.int32, device="cuda")
+    ac = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sv.spec_profile_enable(m.h, True)
+    sv.spec_verify_step(m.h, blk, am, ac)      # warm the direct-launch path
+    sv.spec_kv_rollback(m.h, 0, ctx)
+    sv.spec_profile_read(m.h, sv.PROF_ALL)
+    out = []
+    for _ in range(reps):
+        sv.spec_verify_step(m.h, blk, am, ac)
+        sv.spec_kv_rollback(m.h, 0, ctx)
+        g_ms, g_b, _ = sv.spec_profile_read(m.h, sv.EPI_EXPERT_SWIGLU)
+        d_ms, d_b, _ = sv.spec_profile_read(m.h, sv.EPI_EXPERT_DOWN)
+        sv.spec_profile_read(m.h, sv.PROF_ALL)
+        out.append(((g_ms + d_ms) * 1e-3, g_b + d_b))
+    sv.spec_profile_enable(m.h, False)
+    return out
+
+
 def suite_moe(args):
     """DeepSeek-V2-Lite-shaped MoE verify at n = 1..8 with forced synthetic
-    routing traces: per-slot vs deduplicated expert reads (time, requested
-    bytes, effective bandwidth), the measured and predicted crossover, and the
-    best draft length over 22 acceptance rates."""
+    routing traces, per-slot against deduplicated expert reads, following the
+    MoE page's method (abstract): a step's time is the bytes each kernel
+    requests over its effective bandwidth plus fixed time; the bandwidths are
+    fitted on one layer's expert operation run alone (a two-layer model of
+    the same shapes, launches bracketed by events); bytes from the routing
+    traces over those bandwidths predict the time deduplication saves (with
+    the bound a bandwidth error puts on it), the crossover, and the best
+    draft length over 22 acceptance rates, each beside the measured value."""
     import numpy as np
     import torch
     import synth
@@ -1282,34 +1311,60 @@ def suite_moe(args):
     from speculative_decoding_verify_pass_gb300 import stepmodel
     ctx = 2048
     cfg = synth.moe_v2lite(max_ctx=ctx + 64)
-    plan = sv.layer_skip_plan(cfg.n_layers, 0.5)
-    m, _ = _model_at_context(cfg, ctx, plan)
     L = cfg.n_layers
+    moe_layers = list(range(cfg.first_moe_layer, L))
     trace = synth.routing_trace(L, 16, cfg.n_experts, cfg.top_k)       # [layer][token][k]
-    m.force_routing(trace)
     per_expert = stepmodel.expert_bytes(cfg)
-    # the shared experts are work items of the same launches, read once per pass in both modes
-    shared_bytes = (L - cfg.first_moe_layer) * cfg.n_shared_experts * per_expert
-    rows = {}
-    for n in range(1, 9):
+    S = cfg.n_shared_experts
+    ns = list(range(1, 9))
+    modes = ((sv.SPEC_MOE_PER_SLOT, "per_slot"), (sv.SPEC_MOE_DEDUP, "dedup"))
+
+    def layer_bytes(l, n, name):   # expert bytes one layer's expert operation requests
+        reads = n * cfg.top_k if name == "per_slot" else stepmodel.union_size(trace[l, :n])
+        return (reads + S) * per_expert
+
+    # ---- fit: one layer's expert operation, run alone, at every pass size;
+    # per mode, time = t0 + bytes / B (least squares over all runs) ----
+    one = synth.scaled(cfg, n_layers=cfg.first_moe_layer + 1)
+    m1, _ = _model_at_context(one, ctx)
+    ftrace = np.zeros((one.n_layers, 16, cfg.top_k), dtype=np.int32)
+    ftrace[cfg.first_moe_layer] = trace[cfg.first_moe_layer]
+    m1.force_routing(ftrace)
+    pts = {name: ([], []) for _, name in modes}
+    for n in ns:
         toks = synth.prompt(cfg, n).tolist()
-        u_layers = [stepmodel.union_size(trace[l, :n]) for l in range(cfg.first_moe_layer, L)]
-        for mode, name in ((sv.SPEC_MOE_PER_SLOT, "per_slot"), (sv.SPEC_MOE_DEDUP, "dedup")):
+        for mode, name in modes:
+            m1.moe_mode(mode)
+            runs = _expert_op_runs(torch, sv, m1, toks, ctx, 5)
+            for t, b in runs:
+                pts[name][0].append(b)
+                pts[name][1].append(t)
+            _emit({"suite": "moe_fit_run", "config": "moe-v2-lite", "layer": cfg.first_moe_layer, "n": n,
+                   "mode": name, "expert_op_us": round(float(np.mean([t for t, _ in runs])) * 1e6, 2),
+                   "bytes": int(runs[0][1])})
+    fit = {name: stepmodel.fit_time_model(*pts[name]) for _, name in modes}
+    _emit({"suite": "moe_fit", "model": "t = t0 + bytes / B over one layer's expert operation run alone, n = 1..8",
+           **{name: {"t0_us": round(f[0] * 1e6, 2), "GBps": round(f[1] / 1e9, 1), "rel_err": round(f[2], 4)}
+              for name, f in fit.items()}})
+    m1.close()
+    del m1
+    torch.cuda.empty_cache()
+
+    # ---- measure: the full model ----
+    plan = sv.layer_skip_plan(L, 0.5)
+    m, _ = _model_at_context(cfg, ctx, plan)
+    m.force_routing(trace)
+    shared_bytes = len(moe_layers) * S * per_expert
+    rows = {}
+    for n in ns:
+        toks = synth.prompt(cfg, n).tolist()
+        u_layers = [stepmodel.union_size(trace[l, :n]) for l in moe_layers]
+        for mode, name in modes:
             m.moe_mode(mode)
             us = _verify_us(torch, sv, m, toks, ctx)
-            sv.spec_profile_enable(m.h, True)
-            blk = torch.tensor(toks, dtype=torch.int32, device="cuda")
-            am = torch.zeros(n, dtype=torch.int32, device="cuda")
-            ac = torch.zeros(1, dtype=torch.int32, device="cuda")
-            for _ in range(3):
-                sv.spec_verify_step(m.h, blk, am, ac)
-                sv.spec_kv_rollback(m.h, 0, ctx)
-            g_ms, g_b, g_n = sv.spec_profile_read(m.h, sv.EPI_EXPERT_SWIGLU)
-            d_ms, d_b, d_n = sv.spec_profile_read(m.h, sv.EPI_EXPERT_DOWN)
-            sv.spec_profile_read(m.h, sv.PROF_ALL)
-            sv.spec_profile_enable(m.h, False)
-            exp_us = (g_ms + d_ms) * 1e3 / 3
-            exp_bytes = (g_b + d_b) / 3
+            runs = _expert_op_runs(torch, sv, m, toks, ctx, 3)
+            exp_us = float(np.mean([t for t, _ in runs])) * 1e6
+            exp_bytes = runs[0][1]
             rows[(n, name)] = (us, exp_us, exp_bytes)
             _emit({"suite": "moe", "config": "moe-v2-lite", "ctx": ctx, "n": n, "mode": name,
                    "verify_us": round(us, 1), "expert_us": round(exp_us, 1),
@@ -1317,32 +1372,67 @@ def suite_moe(args):
                    "expert_GBps": round(exp_bytes / exp_us / 1e3, 1),
                    "unique_experts_mean": round(float(np.mean(u_layers)), 2),
                    "unique_experts_expected": round(stepmodel.union_size_expected(n, cfg.n_experts, cfg.top_k), 2)})
-    # crossover: measured (verify time) and predicted (bytes over bandwidths fitted at one pass size)
-    ns = list(range(1, 9))
-    fit_n = 4
-    b_ps = rows[(fit_n, "per_slot")][2] / rows[(fit_n, "per_slot")][1]
-    b_dd = rows[(fit_n, "dedup")][2] / rows[(fit_n, "dedup")][1]
-    shares = [rows[(n, "dedup")][2] / rows[(n, "per_slot")][2] for n in ns]
-    ratios = [(rows[(n, "dedup")][2] / rows[(n, "dedup")][1]) / (rows[(n, "per_slot")][2] / rows[(n, "per_slot")][1])
+
+    # ---- predictions: trace bytes of every MoE layer through the fitted model ----
+    def expert_time(n, name, scale=1.0):   # seconds, every MoE layer of the pass
+        t0, bw, _ = fit[name]
+        return stepmodel.model_time(t0, bw * scale, [layer_bytes(l, n, name) for l in moe_layers])
+
+    (_, _, e_ps), (_, _, e_dd) = fit["per_slot"], fit["dedup"]
+    saving = []
+    for n in ns:
+        t_ps, t_dd = expert_time(n, "per_slot"), expert_time(n, "dedup")
+        bound = t_ps * e_ps / (1.0 - e_ps) + t_dd * e_dd / (1.0 - e_dd)
+        meas = (rows[(n, "per_slot")][0] - rows[(n, "dedup")][0]) * 1e-6
+        bps = sum(layer_bytes(l, n, "per_slot") for l in moe_layers)
+        bdd = sum(layer_bytes(l, n, "dedup") for l in moe_layers)
+        saving.append({"n": n, "byte_share_u": round(bdd / bps, 4),
+                       "r_fit": round((bdd / t_dd) / (bps / t_ps), 4),
+                       "saving_pred_us": round((t_ps - t_dd) * 1e6, 1), "bound_us": round(bound * 1e6, 1),
+                       "saving_meas_us": round(meas * 1e6, 1), "inside_bound": abs(meas - (t_ps - t_dd)) <= bound})
+    _emit({"suite": "moe_saving", "points": saving,
+           "inside": sum(x["inside_bound"] for x in saving)})
+    shares = [x["byte_share_u"] for x in saving]
+    r_fit = [x["r_fit"] for x in saving]
+    r_meas = [(rows[(n, "dedup")][2] / rows[(n, "dedup")][1]) / (rows[(n, "per_slot")][2] / rows[(n, "per_slot")][1])
               for n in ns]
     measured = next((n for n in ns if rows[(n, "dedup")][0] < rows[(n, "per_slot")][0]), None)
-    predicted = stepmodel.first_win(ns, shares, [b_dd / b_ps] * len(ns))
-    _emit({"suite": "moe_crossover", "byte_share_u": [round(x, 3) for x in shares],
-           "bandwidth_ratio_r": [round(x, 3) for x in ratios], "fit_pass_size": fit_n,
-           "r_fit": round(b_dd / b_ps, 3), "crossover_measured": measured, "crossover_predicted": predicted})
-    # best draft length over 22 acceptance rates (verify in the faster mode per n; draft = 50% middle skip)
+    predicted = stepmodel.first_win(ns, shares, r_fit)
+    _emit({"suite": "moe_crossover", "byte_share_u": shares, "r_fit_one_layer_alone": r_fit,
+           "r_in_pass": [round(x, 3) for x in r_meas], "crossover_measured": measured,
+           "crossover_predicted": predicted})
+
+    # ---- best draft length: from measured verify times, and predicted from
+    # operation times (a plain one-token step, the fitted expert operation)
     m.moe_mode(sv.SPEC_MOE_DEDUP)
-    t_draft = _draft_us(torch, sv, m, ctx)
-    tv = {n: min(rows[(n, "per_slot")][0], rows[(n, "dedup")][0]) for n in ns}
+    t_draft = _draft_us(torch, sv, m, ctx) * 1e-6
+    tv_meas = {n: min(rows[(n, "per_slot")][0], rows[(n, "dedup")][0]) * 1e-6 for n in ns}
+    pv = {name: stepmodel.predicted_verify_times(rows[(1, name)][0] * 1e-6, lambda n, nm=name: expert_time(n, nm), ns)
+          for _, name in modes}
+    tv_pred = {n: min(pv["per_slot"][n], pv["dedup"][n]) for n in ns}
+    alphas = np.linspace(0.0, 1.0, 22)
     gam = list(range(0, 8))
-    stairs, stairs0 = [], []
-    for a in np.linspace(0.0, 1.0, 22):
-        stairs.append(stepmodel.best_gamma(float(a), lambda k: tv[k], t_draft, gam))
-        stairs0.append(stepmodel.best_gamma(float(a), lambda k: tv[k], 0.0, gam))
-    _emit({"suite": "moe_best_gamma", "draft_us": round(t_draft, 1), "alphas": 22,
-           "best_gamma": stairs, "best_gamma_free_draft": stairs0,
-           "monotone": all(b >= a for a, b in zip(stairs, stairs[1:])),
-           "monotone_free_draft": all(b >= a for a, b in zip(stairs0, stairs0[1:]))})
+    st_meas = stepmodel.gamma_staircase(alphas, lambda k: tv_meas[k], t_draft, gam)
+    st_pred = stepmodel.gamma_staircase(alphas, lambda k: tv_pred[k], t_draft, gam)
+    # how a bandwidth error moves the staircase: every fitted bandwidth at the
+    # low and at the high end of its error
+    spread = []
+    for sgn in (-1.0, 1.0):
+        pvs = {name: stepmodel.predicted_verify_times(
+                   rows[(1, name)][0] * 1e-6, lambda n, nm=name, sg=sgn: expert_time(n, nm, 1.0 + sg * fit[nm][2]), ns)
+               for _, name in modes}
+        spread.append(stepmodel.gamma_staircase(alphas, lambda k: min(pvs["per_slot"][k], pvs["dedup"][k]),
+                                                t_draft, gam))
+    st_free = stepmodel.gamma_staircase(alphas, lambda k: tv_meas[k], 0.0, gam)
+    _emit({"suite": "moe_best_gamma", "draft_us": round(t_draft * 1e6, 1), "alphas": 22,
+           "best_gamma_measured": st_meas, "best_gamma_predicted": st_pred,
+           "best_gamma_predicted_bw_low": spread[0], "best_gamma_predicted_bw_high": spread[1],
+           "within_one": sum(abs(a - b) <= 1 for a, b in zip(st_meas, st_pred)),
+           "best_gamma_measured_free_draft": st_free,
+           "monotone_measured": all(b >= a for a, b in zip(st_meas, st_meas[1:])),
+           "monotone_predicted": all(b >= a for a, b in zip(st_pred, st_pred[1:])),
+           "verify_us_measured": {n: round(tv_meas[n] * 1e6, 1) for n in ns},
+           "verify_us_predicted": {n: round(tv_pred[n] * 1e6, 1) for n in ns}})
     m.close()
 
 

@@ -131,3 +131,24 @@ def predicted_verify_times(t_plain: float, expert_time, pass_sizes):
 def gamma_staircase(alphas, verify_time, draft_time: float, gammas):
     """Best draft length for each acceptance rate."""
     return [best_gamma(float(a), verify_time, draft_time, gammas) for a in alphas]
+
+
+def fit_time_model(byte_counts, seconds):
+    """Least-squares fit of an operation's time as fixed time plus bytes over
+    effective bandwidth, t = t0 + bytes / B, over runs of different byte
+    counts.  Returns (t0, B, rel_err) with rel_err the largest relative
+    residual |t - t0 - bytes/B| / t of the runs, used as the model's error."""
+    n = len(byte_counts)
+    mb = sum(byte_counts) / n
+    mt = sum(seconds) / n
+    sxx = sum((b - mb) ** 2 for b in byte_counts)
+    sxy = sum((b - mb) * (t - mt) for b, t in zip(byte_counts, seconds))
+    slope = sxy / sxx
+    t0 = mt - slope * mb
+    err = max(abs(t - t0 - slope * b) / t for b, t in zip(byte_counts, seconds))
+    return t0, 1.0 / slope, err
+
+
+def model_time(t0: float, bandwidth: float, byte_counts) -> float:
+    """Summed time of operations of the given byte counts under the fit."""
+    return sum(t0 + b / bandwidth for b in byte_counts)

@@ -142,3 +142,16 @@ def test_step_model_predictions_from_fitted_bandwidths():
     assert tv[1] == 1000.0 and tv[8] == 1000.0 + 280.0
     st = sm.gamma_staircase(np.linspace(0.0, 1.0, 22), lambda n: tv[n], 300.0, range(0, 8))
     assert st[0] == 0 and all(b >= a for a, b in zip(st, st[1:]))
+
+
+def test_step_model_affine_fit():
+    """t = t0 + bytes / B recovered from exact points; the relative error is
+    the largest residual; the summed model time of several operations."""
+    from speculative_decoding_verify_pass_gb300 import stepmodel as sm
+    b = [1e9, 2e9, 3e9, 4e9]
+    t0, bw, err = sm.fit_time_model(b, [6e-4 + x / 2e12 for x in b])
+    assert abs(t0 - 6e-4) < 1e-12 and abs(bw - 2e12) / 2e12 < 1e-9 and err < 1e-9
+    t0, bw, err = sm.fit_time_model(b, [1.0e-3, 1.7e-3, 2.0e-3, 2.6e-3])
+    resid = [abs(t - t0 - x / bw) / t for x, t in zip(b, [1.0e-3, 1.7e-3, 2.0e-3, 2.6e-3])]
+    assert abs(err - max(resid)) < 1e-12 and err > 0.01
+    assert abs(sm.model_time(1e-4, 1e12, [1e9, 3e9]) - (2e-4 + 4e-3)) < 1e-15
