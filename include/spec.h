@@ -268,6 +268,34 @@ spec_status spec_batch_len(spec_handle h, int32_t seq, int32_t* out_len);
 spec_status spec_verify_batch(spec_handle h, const int32_t* d_blocks, int32_t nseq, int32_t n, int32_t* d_argmax,
                               int32_t* d_accept, float* d_logits_opt);
 
+/* Sampled verification (LayerSkip summary, 4.3.2 "Self-Verification": with
+ * sampling, rejection sampling keeps the output distribution exactly the full
+ * model's; the pages give the property, and the rule here is the standard
+ * one of speculative sampling).  With p_j = softmax(target_logits[j] / T) and
+ * q_j = softmax(draft_logits[j] / T), the draft x = d_block[j+1] (drawn from
+ * q_j by the caller) is accepted when u_j * q_j(x) < p_j(x), tested in the log
+ * domain from the logits; at the first rejection j the next token is drawn
+ * from norm(max(0, p_j - q_j)) (from p_j where p_j == q_j), after a full
+ * accept from p_{n-1}.  A draw with uniform u is the smallest index whose
+ * running weight sum exceeds u times the total.
+ *   d_target_logits  float32 [n][vocab] (e.g. spec_verify_step's logits);
+ *   d_draft_logits   float32 [n-1][vocab] (e.g. spec_draft_step_logits'
+ *                    rows), NULL only when n == 1;
+ *   d_block          int32 [n]: the last accepted token, then the drafts;
+ *   n                1..16; with n == 1 the call draws one token from p_0
+ *                    (plain sampling, or a draft's own proposal);
+ *   temperature      > 0 and finite;
+ *   d_uniforms       float64 [n] in [0, 1): u_0 .. u_{n-2} for the accept
+ *                    tests, then the draw's; CALLER-supplied, so a run is
+ *                    reproducible and the random source is the caller's;
+ *   d_accept_len[0]  the number of accepted drafts k;
+ *   d_next_token[0]  the token drawn at position k.
+ * Uses the handle's scratch (four small launches on its stream); the vocab
+ * is the handle's.  Argument errors: SPEC_ERR_INVALID_ARG, nothing enqueued. */
+spec_status spec_accept_sampled(spec_handle h, const float* d_target_logits, const float* d_draft_logits,
+                                const int32_t* d_block, int32_t n, float temperature, const double* d_uniforms,
+                                int32_t* d_accept_len, int32_t* d_next_token);
+
 /* Thread-local description of the last error. */
 const char* spec_last_error(void);
 

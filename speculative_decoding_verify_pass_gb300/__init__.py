@@ -29,7 +29,7 @@ EXPORTED = ["spec_model_create", "spec_model_destroy", "spec_set_draft_plan", "s
             "spec_accept_from_logits_noalloc", "spec_trace_enable", "spec_trace_read", "spec_trace_kinds",
             "spec_set_taps", "spec_set_context_fc", "spec_context_append", "spec_batch_reserve",
             "spec_batch_kv_load", "spec_batch_kv_export", "spec_batch_set_len", "spec_batch_len",
-            "spec_verify_batch", "spec_share_prefix", "spec_draft_step_logits"]
+            "spec_verify_batch", "spec_share_prefix", "spec_draft_step_logits", "spec_accept_sampled"]
 
 
 class SpecError(RuntimeError):
@@ -81,6 +81,7 @@ def library():
         "spec_prefill": [vp, vp, i32, vp],
         "spec_draft_step": [vp, vp, i32, vp],
         "spec_draft_step_logits": [vp, vp, i32, vp, vp],
+        "spec_accept_sampled": [vp, vp, vp, vp, i32, ctypes.c_float, vp, vp, vp],
         "spec_verify_step": [vp, vp, i32, vp, vp, vp, vp, vp],
         "spec_kv_rollback": [vp, i32, i32],
         "spec_moe_mode": [vp, i32],
@@ -152,6 +153,15 @@ def spec_draft_step_logits(h, d_tokens, d_draft_token, d_logits=None):
 def spec_verify_step(h, d_block, d_argmax, d_accept_len, d_logits=None, d_expert_ids=None, d_next_pair=None):
     _check(library().spec_verify_step(h, _ptr(d_block), int(d_block.numel()), _ptr(d_argmax), _ptr(d_accept_len),
                                       _ptr(d_logits), _ptr(d_expert_ids), _ptr(d_next_pair)))
+
+
+def spec_accept_sampled(h, d_target_logits, d_draft_logits, d_block, temperature, d_uniforms, d_accept_len,
+                        d_next_token):
+    """Rejection-sampling accept: target logits [n][V], draft logits [n-1][V]
+    (None for n == 1), block int32 [n], uniforms float64 [n]."""
+    _check(library().spec_accept_sampled(h, _ptr(d_target_logits), _ptr(d_draft_logits), _ptr(d_block),
+                                         int(d_block.numel()), float(temperature), _ptr(d_uniforms),
+                                         _ptr(d_accept_len), _ptr(d_next_token)))
 
 
 def spec_kv_rollback(h, which: int, new_len: int):
@@ -408,6 +418,16 @@ class Model:
     def rollback(self, which, new_len):
         spec_kv_rollback(self.h, which, new_len)
 
+    def accept_sampled(self, target_logits, draft_logits, d_block, temperature, uniforms):
+        """(accept_len, next token) device tensors of the rejection-sampling
+        accept; uniforms: n float64 values (host or device)."""
+        torch = self._torch
+        u = torch.as_tensor(uniforms, dtype=torch.float64).to("cuda")
+        acc = self._i32(1)
+        tok = self._i32(1)
+        spec_accept_sampled(self.h, target_logits, draft_logits, d_block, temperature, u, acc, tok)
+        return acc, tok
+
     def kv_len(self, which):
         return spec_kv_len(self.h, which)
 
@@ -558,6 +578,54 @@ class Model:
             dlen = min(pos + k + 1, dlen)
             self.rollback(SPEC_CACHE_DRAFT, dlen)
         return out[:max_new], accepts
+
+
+def selfspec_sampled(model, prompt, max_new, gamma, temperature, uniforms):
+    """Self-speculative decoding with sampling: the draft samples each
+    proposal from its own distribution at `temperature`, the target verifies
+    the block by rejection sampling (spec_accept_sampled), both caches are
+    rolled back to the accepted length.  ``uniforms(cycle, count)`` returns the
+    float64 uniforms a cycle draws (gamma draft draws, then gamma accept tests
+    and the final draw).  The prompt's last token is the first block's head.
+    Returns (tokens, accept lengths)."""
+    import torch
+    m = model
+    p = [int(t) for t in prompt]
+    one = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.prefill(p[:-1])
+    seq = list(p)
+    out, accepts = [], []
+    dlen = len(p) - 1
+    cycle = 0
+    while len(out) < max_new:
+        pos = len(seq) - 1
+        u = list(uniforms(cycle, 2 * gamma + 1))
+        feed = seq[dlen:pos + 1]
+        drafts, dlog = [], []
+        for i in range(gamma):
+            t = torch.tensor(feed, dtype=torch.int32, device="cuda")
+            _, lg = m.draft_step(t, logits=True)
+            row = lg[-1:].contiguous()
+            _, x = m.accept_sampled(row, None, one, temperature, [u[i]])
+            d = int(x.item())
+            dlen += len(feed)
+            drafts.append(d)
+            dlog.append(row)
+            feed = [d]
+        block = torch.tensor([seq[pos]] + drafts, dtype=torch.int32, device="cuda")
+        _, _, tl, _ = m.verify(block, logits=True)
+        dl = torch.cat(dlog, 0) if dlog else None
+        k, tok = m.accept_sampled(tl, dl, block, temperature, u[gamma:])
+        k = int(k.item())
+        emitted = drafts[:k] + [int(tok.item())]
+        accepts.append(k)
+        out += emitted
+        seq += emitted
+        m.rollback(SPEC_CACHE_TARGET, pos + k + 1)
+        dlen = min(pos + k + 1, dlen)
+        m.rollback(SPEC_CACHE_DRAFT, dlen)
+        cycle += 1
+    return out[:max_new], accepts
 
 
 def layer_skip_plan(n_layers: int, skip_frac: float):

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["gemm.cu", "attention.cu", "misc.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["gemm.cu", "attention.cu", "misc.cu", "api.cu", "noalloc.cu", "sampling.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -131,6 +131,10 @@ struct spec_model {
     std::vector<ProfRec> prof;
     std::vector<void*> allocs;
     std::vector<void*> draft_allocs;
+    float2* samp_stats = nullptr;       // sampled verification scratch (sampling.cu)
+    double2* samp_rows = nullptr;
+    double* samp_sums = nullptr;
+    int* samp_decision = nullptr;
     bool share_prefix = false;          // the draft's leading layers 0..n_shared-1 use the target's caches
     int n_shared = 0;                   // layers the draft plan shares with the target as a contiguous prefix
 };
@@ -832,6 +836,13 @@ spec_status spec_model_create(const spec_model_config* cfg, const spec_weights* 
     TRY(dalloc_t(h, &h->amax_val, (size_t)kMaxBlock * h->lm.T));
     TRY(dalloc_t(h, &h->amax_idx, (size_t)kMaxBlock * h->lm.T));
     TRY(dalloc_t(h, &h->st, 1));
+    {
+        const int ch = sample_chunks(c.vocab);
+        TRY(dalloc_t(h, &h->samp_stats, (size_t)(2 * kMaxBlock - 1) * ch));
+        TRY(dalloc_t(h, &h->samp_rows, (size_t)(2 * kMaxBlock - 1)));
+        TRY(dalloc_t(h, &h->samp_sums, (size_t)2 * ch));
+        TRY(dalloc_t(h, &h->samp_decision, 2));
+    }
     if (c.n_experts > 0) {
         const int K = c.top_k;
         TRY(dalloc_t(h, &h->route_ids, (size_t)kMaxBlock * K));
@@ -933,6 +944,36 @@ spec_status spec_verify_step(spec_handle h, const int32_t* d_block, int32_t n, i
                  nullptr, d_block);
     if (s == SPEC_OK) h->host_len[0] += n;
     return s;
+}
+
+spec_status spec_accept_sampled(spec_handle h, const float* d_target_logits, const float* d_draft_logits,
+                                const int32_t* d_block, int32_t n, float temperature, const double* d_uniforms,
+                                int32_t* d_accept_len, int32_t* d_next_token) {
+    if (!h || !d_target_logits || !d_block || !d_uniforms || !d_accept_len || !d_next_token)
+        return fail(SPEC_ERR_INVALID_ARG, "null argument");
+    if (n < 1 || n > SPEC_MAX_BLOCK) return fail(SPEC_ERR_INVALID_ARG, "block size %d outside 1..16", n);
+    if (n > 1 && !d_draft_logits) return fail(SPEC_ERR_INVALID_ARG, "draft logits needed for n > 1");
+    if (!(temperature > 0.f) || !std::isfinite(temperature))
+        return fail(SPEC_ERR_INVALID_ARG, "temperature must be positive and finite");
+    SampleParams p{};
+    p.target = d_target_logits;
+    p.draft = n > 1 ? d_draft_logits : nullptr;
+    p.block = d_block;
+    p.uniforms = d_uniforms;
+    p.n = n;
+    p.vocab = h->c.vocab;
+    p.chunks = sample_chunks(h->c.vocab);
+    p.temperature = temperature;
+    p.stats = h->samp_stats;
+    p.row_stat = h->samp_rows;
+    p.chunk_sum = h->samp_sums;
+    p.decision = h->samp_decision;
+    p.out_accept = d_accept_len;
+    p.out_token = d_next_token;
+    h->launches = 0;
+    CU(launch_sample_accept(p, h->stream, h->pdl));
+    h->launches = 4;
+    return SPEC_OK;
 }
 
 spec_status spec_kv_rollback(spec_handle h, int32_t which, int32_t new_len) {

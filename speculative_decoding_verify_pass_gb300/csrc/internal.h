@@ -212,6 +212,25 @@ cudaError_t launch_pack(const PackSrc& s, const PackedMat& m, cudaStream_t st);
 cudaError_t launch_kv_io(uint16_t* pool, const int* block_table, uint16_t* logical, int ctx, int hkv, int hd,
                          bool to_pool, cudaStream_t s);
 
+// Sampled verification (sampling.cu): rejection-sampling accept from the
+// target's and the draft's logits and caller-supplied uniforms.
+struct SampleParams {
+    const float* target;       // [n][vocab] target logits
+    const float* draft;        // [n-1][vocab] draft logits (null when n == 1)
+    const int* block;          // [n]: last accepted token, then the drafts
+    const double* uniforms;    // [n]: one per accept test, then the draw's
+    int n, vocab, chunks;
+    float temperature;
+    float2* stats;             // [2n-1][chunks] (max of l/T, sum of exp(l/T - max)) per chunk
+    double2* row_stat;         // [2n-1] (max, log of the sum) per row
+    double* chunk_sum;         // [2][chunks] the draw's weight sums per chunk (and p's)
+    int* decision;             // [2]: row k of the draw, and 1 (from p) or 0 (residual)
+    int* out_accept;
+    int* out_token;
+};
+int sample_chunks(int vocab);
+cudaError_t launch_sample_accept(const SampleParams& p, cudaStream_t s, bool pdl);
+
 // Sets the thread-local message returned by spec_last_error (api.cu).
 void set_last_error(const char* msg);
 
