@@ -310,13 +310,15 @@ __device__ __forceinline__ void attn_unit_c(const AttnParams& a, const uint16_t*
 // projection's operand.  Each lane owns HD/32 consecutive dimensions.  The
 // first kFirst chunks' partial outputs are loaded together with the chunk
 // statistics (their addresses do not depend on them), so a row of up to
-// kFirst chunks costs one round trip to L2.  Every lane reads every chunk's
+// kFirst chunks costs one round trip to L2 and issues no load after it: the
+// next GEMM's weight prefetch starts with this kernel, and a load queued
+// behind it waits microseconds.  Every lane reads every chunk's
 // (max, sum) (uniform loads) and forms the same weights; the sums run in
 // chunk order, so a row's result does not depend on the block size.
 template <int HD>
 __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep, int lane, int nc) {
     constexpr int V = HD / 32;   // dimensions per lane: 4 (hd 128) or 2 (hd 64)
-    constexpr int kFirst = 24;
+    constexpr int kFirst = 20;
     const int G = a.n_heads / a.n_kv_heads;
     const int nseq = a.seq_len ? a.nseq : 1;
     const int per = a.n_heads * a.n;            // rows of one sequence
@@ -336,11 +338,10 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
         const size_t sbase = (size_t)sq * a.n_kv_heads * a.nch * 64;
         const float2* ml = a.part_ml + sbase + (size_t)h * a.nch * 64 + r;
         const float* po = a.part_o + (sbase + (size_t)h * a.nch * 64 + r) * HD + lane * V;
-        // the first kFirst chunks' outputs and row maxima in one sweep of
-        // independent loads (one L2 round trip), later chunks' maxima after;
-        // the row sums are read again below, from lines this sweep brought in
+        // the first kFirst chunks' outputs and (max, sum) in one sweep of
+        // independent loads (one L2 round trip), later chunks' maxima after
         float ob[kFirst][V];
-        float mf[kFirst];
+        float2 sf[kFirst];
 #pragma unroll
         for (int t = 0; t < kFirst; ++t) {
             if (t < nc) {
@@ -351,13 +352,13 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
                     const float2 v = *reinterpret_cast<const float2*>(po + (size_t)t * cstride);
                     ob[t][0] = v.x; ob[t][1] = v.y;
                 }
-                mf[t] = ml[(size_t)t * 64].x;
+                sf[t] = ml[(size_t)t * 64];
             }
         }
         float M = -1e30f;
 #pragma unroll
         for (int t = 0; t < kFirst; ++t)
-            if (t < nc) M = fmaxf(M, mf[t]);
+            if (t < nc) M = fmaxf(M, sf[t].x);
         for (int c0 = kFirst; c0 < nc; c0 += 8) {   // longer rows: eight statistics loads in flight
             float m[8];
 #pragma unroll
@@ -371,7 +372,7 @@ __device__ __forceinline__ void comb_rows(const AttnParams& a, int u0, int ustep
 #pragma unroll
         for (int t = 0; t < kFirst; ++t) {
             if (t < nc) {
-                const float2 st = ml[(size_t)t * 64];
+                const float2 st = sf[t];
                 const float w = exp2f(st.x - M);
                 L += w * st.y;
 #pragma unroll
