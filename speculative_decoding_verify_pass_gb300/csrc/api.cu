@@ -1072,9 +1072,9 @@ static spec_status batch_kv_io(spec_handle h, int32_t seq, int32_t slot, void* d
     if (ctx < 0 || ctx > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "ctx %d out of range", ctx);
     const size_t off = h->pool_elems * ((size_t)h->bat_cap * slot + seq);   // the sequence's own pages
     CU(launch_kv_io(h->kb + off, h->block_table, static_cast<uint16_t*>(dk), ctx, h->c.n_kv_heads, h->c.head_dim, load,
-                    h->stream));
+                    false, h->stream));
     CU(launch_kv_io(h->vb + off, h->block_table, static_cast<uint16_t*>(dv), ctx, h->c.n_kv_heads, h->c.head_dim, load,
-                    h->stream));
+                    true, h->stream));
     return SPEC_OK;
 }
 
@@ -1235,8 +1235,10 @@ static spec_status kv_io(spec_handle h, int32_t which, int32_t slot, void* dk, v
     if (ctx < 0 || ctx > h->c.max_ctx) return fail(SPEC_ERR_INVALID_ARG, "ctx %d out of range", ctx);
     uint16_t* kp = kv_pool(h, which, slot, 0);
     uint16_t* vp = kv_pool(h, which, slot, 1);
-    CU(launch_kv_io(kp, h->block_table, static_cast<uint16_t*>(dk), ctx, h->c.n_kv_heads, h->c.head_dim, load, h->stream));
-    CU(launch_kv_io(vp, h->block_table, static_cast<uint16_t*>(dv), ctx, h->c.n_kv_heads, h->c.head_dim, load, h->stream));
+    CU(launch_kv_io(kp, h->block_table, static_cast<uint16_t*>(dk), ctx, h->c.n_kv_heads, h->c.head_dim, load, false,
+                    h->stream));
+    CU(launch_kv_io(vp, h->block_table, static_cast<uint16_t*>(dv), ctx, h->c.n_kv_heads, h->c.head_dim, load, true,
+                    h->stream));
     return SPEC_OK;
 }
 

@@ -68,11 +68,18 @@ __host__ __device__ __forceinline__ long long x_kblock_stride(int f32) {
     return f32 ? (long long)kStageX32Bytes : (long long)kStageXBytes;
 }
 
-// Element offset of (key slot, dim) inside one KV page slab [64][hd]: 16-byte
-// chunks of a row are XOR-permuted by (slot & 7), so the attention kernel's
-// fragment loads from the bulk-copied slab hit distinct shared-memory banks.
-__device__ __forceinline__ int kv_swz(int slot, int dim, int hd) {
-    return slot * hd + ((((dim >> 3) ^ (slot & 7))) << 3) + (dim & 7);
+// Element offsets of (key slot, dim) inside one KV page slab (64 positions of
+// one kv head, hd dims), in the tensor core's canonical K-major layout: core
+// matrices of 8 rows x 8 bf16 (128 contiguous bytes).  K is the key operand
+// of S = Q K^T (rows = positions, k = dims): [8-position group][8-dim
+// group][position][8 dims].  V is the value operand of O = P V (rows = dims,
+// k = positions): [8-dim group][8-position group][dim][8 positions].  A
+// bulk-copied slab is an MMA operand as it lies.
+__host__ __device__ __forceinline__ int kv_off_k(int slot, int dim, int hd) {
+    return ((((slot >> 3) * (hd >> 3)) + (dim >> 3)) << 6) + ((slot & 7) << 3) + (dim & 7);
+}
+__host__ __device__ __forceinline__ int kv_off_v(int slot, int dim) {
+    return ((((dim >> 3) << 3) + (slot >> 3)) << 6) + ((dim & 7) << 3) + (slot & 7);
 }
 
 // ----------------------------------------------------------- PTX helpers ---
@@ -212,9 +219,18 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
            (1ull << 46);
 }
 
+// The same for any core-matrix strides: lbo along k, sbo per 8-row group.
+__device__ __forceinline__ uint64_t umma_desc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+           (1ull << 46);
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both
-// operands K-major, M = 128 (bits 24..28: M >> 4), N = 16 (bits 17..22: N >> 3).
-constexpr uint32_t kUmmaIdescM128N16 = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+// operands K-major: M (bits 24..28: M >> 4) x N (bits 17..22: N >> 3).
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(uint32_t m, uint32_t n) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+constexpr uint32_t kUmmaIdescM128N16 = umma_idesc_bf16(128, 16);
 
 // D[tmem] (+)= A[128 x 16] * B[16 x 16]^T; accumulate = 0 starts from zero.
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
@@ -222,6 +238,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(kUmmaIdescM128N16), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= A * B^T under instruction descriptor idesc.
+__device__ __forceinline__ void umma_bf16_id(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -281,6 +307,53 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 4 consecutive fp32 columns of this warp's 32 TMEM lanes, waiting for the
+// load; and the matching store.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+    uint32_t r[4];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const float (&v)[4]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n\t"
+        "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3]))
+        : "memory");
+}
+
+// 2^x by the hardware's approximate base-2 exponential (one instruction;
+// results below the smallest normal flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Sum of v over the 32 lanes of a warp (integer: exact, in no particular order).
+__device__ __forceinline__ uint32_t warp_sum_u32(uint32_t v) {
+    uint32_t r;
+    asm volatile("redux.sync.add.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+    return r;
+}
+
+// Exact maximum of v over the 32 lanes of a warp: floats mapped to ints in
+// the same order (negative values' magnitude bits flipped), one integer
+// warp reduction, mapped back.
+__device__ __forceinline__ float warp_max_exact(float v) {
+    int k = __float_as_int(v);
+    k = k >= 0 ? k : k ^ 0x7FFFFFFF;
+    int m;
+    asm volatile("redux.sync.max.s32 %0, %1, 0xffffffff;" : "=r"(m) : "r"(k));
+    return __int_as_float(m >= 0 ? m : m ^ 0x7FFFFFFF);
+}
+
 // D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -301,12 +374,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
 }
 __device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                 : "r"(addr));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -228,8 +228,8 @@ __device__ __forceinline__ void epilogue(const GemmParams& p, GemmSmem& sm, int 
                 const int slot = pos % kPageSize;
                 uint16_t* base =
                     (isk ? p.kpool : p.vpool) + ((size_t)(page[u] * p.n_kv_heads + kvh) * kPageSize) * hd;
-                base[kv_swz(slot, i, hd)] = f2bf(va);
-                base[kv_swz(slot, i + half, hd)] = f2bf(vb);
+                base[isk ? kv_off_k(slot, i, hd) : kv_off_v(slot, i)] = f2bf(va);
+                base[isk ? kv_off_k(slot, i + half, hd) : kv_off_v(slot, i + half)] = f2bf(vb);
             }
         }
     } else if constexpr (EPI == EPI_RESID) {

@@ -208,9 +208,10 @@ struct PackSrc {
 };
 cudaError_t launch_pack(const PackSrc& s, const PackedMat& m, cudaStream_t st);
 
-// Logical [ctx][Hkv][hd] bf16 <-> paged, swizzled pool.
+// Logical [ctx][Hkv][hd] bf16 <-> paged pool in the K (is_v false) or V
+// page layout (kv_off_k / kv_off_v).
 cudaError_t launch_kv_io(uint16_t* pool, const int* block_table, uint16_t* logical, int ctx, int hkv, int hd,
-                         bool to_pool, cudaStream_t s);
+                         bool to_pool, bool is_v, cudaStream_t s);
 
 // Sampled verification (sampling.cu): rejection-sampling accept from the
 // target's and the draft's logits and caller-supplied uniforms.

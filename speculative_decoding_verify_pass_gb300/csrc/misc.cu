@@ -292,14 +292,17 @@ __global__ void pack_kernel(PackSrc s, uint8_t* out, int N, int T, int KBs) {
     }
 }
 
-__global__ void kv_io_kernel(uint16_t* pool, const int* bt, uint16_t* logical, int ctx, int hkv, int hd, int to_pool) {
+__global__ void kv_io_kernel(uint16_t* pool, const int* bt, uint16_t* logical, int ctx, int hkv, int hd, int to_pool,
+                             int is_v) {
     const long long total = (long long)ctx * hkv * hd;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
         const int dim = (int)(i % hd);
         const int h = (int)((i / hd) % hkv);
         const int pos = (int)(i / ((long long)hd * hkv));
-        const size_t pi = ((size_t)(bt[pos / kPageSize] * hkv + h) * kPageSize) * hd + kv_swz(pos % kPageSize, dim, hd);
+        const int slot = pos % kPageSize;
+        const size_t pi = ((size_t)(bt[pos / kPageSize] * hkv + h) * kPageSize) * hd +
+                          (is_v ? kv_off_v(slot, dim) : kv_off_k(slot, dim, hd));
         if (to_pool)
             pool[pi] = logical[i];
         else
@@ -359,12 +362,12 @@ cudaError_t launch_pack(const PackSrc& src, const PackedMat& m, cudaStream_t st)
 }
 
 cudaError_t launch_kv_io(uint16_t* pool, const int* bt, uint16_t* logical, int ctx, int hkv, int hd, bool to_pool,
-                         cudaStream_t s) {
+                         bool is_v, cudaStream_t s) {
     const long long total = (long long)ctx * hkv * hd;
     if (total == 0) return cudaSuccess;
     long long blocks = (total + 255) / 256;
     if (blocks > 65535) blocks = 65535;
-    kv_io_kernel<<<(unsigned)blocks, 256, 0, s>>>(pool, bt, logical, ctx, hkv, hd, to_pool ? 1 : 0);
+    kv_io_kernel<<<(unsigned)blocks, 256, 0, s>>>(pool, bt, logical, ctx, hkv, hd, to_pool ? 1 : 0, is_v ? 1 : 0);
     return cudaGetLastError();
 }
 
