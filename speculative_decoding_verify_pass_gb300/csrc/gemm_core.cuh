@@ -48,6 +48,8 @@ struct __align__(128) GemmSmem {
     int pos0;                  // cache length at the pass's start (first new position)
     int n_items;
     int emask[kMaxExperts];    // dedup work list: tokens routed to each expert
+    int eidx[kMaxExperts];     // and each present expert's item
+    unsigned eball[2];         // experts present, by warp of 32
     Item items[kMaxItems];
 };
 
@@ -90,9 +92,14 @@ struct StageIter {
             it = (long long)blockIdx.x * I / p.grid;
             end = (long long)(blockIdx.x + 1) * I / p.grid;
         } else {
-            u = blockIdx.x;
+            // k = ceil(U / grid) units per CTA, on the fewest CTAs that hold
+            // them at k each: no CTA runs a second round alone while others
+            // idle (176 units on 152 CTAs: 88 CTAs take 2 each)
             U = n_items * p.T;
-            step = p.grid;
+            const int per = (U + p.grid - 1) / p.grid;
+            const int active = per ? (U + per - 1) / per : 0;
+            step = active;
+            u = (int)blockIdx.x < active ? (int)blockIdx.x : U;
         }
         valid = next_seg();
     }
@@ -136,27 +143,32 @@ __device__ __forceinline__ void build_items(const GemmParams& p, GemmSmem& sm, i
         }
         return;
     }
-    for (int e = tid; e < kMaxExperts; e += nthreads) {   // tokens routed to expert e
-        int mask = 0;
-        for (int i = 0; i < nk; ++i)
-            if ((ids[i] & 63) == e) mask |= 1 << (i / k);
-        sm.emask[e] = mask;
+    // dedup, every step one pass of independent threads: the tokens routed
+    // to each expert (shared-memory ORs), each present expert's place in
+    // ascending id (a ballot over the 64 experts), then each (token, rank)'s slot
+    for (int e = tid; e < kMaxExperts; e += nthreads) sm.emask[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < nk; i += nthreads) atomicOr(&sm.emask[ids[i] & 63], 1 << (i / k));
+    __syncthreads();
+    if (tid < kMaxExperts) {   // kMaxExperts = 64: two warps
+        const bool present = sm.emask[tid] != 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, present);
+        if ((tid & 31) == 0) sm.eball[tid >> 5] = bal;
     }
     __syncthreads();
-    for (int e = tid; e < kMaxExperts; e += nthreads) {
-        if (!sm.emask[e]) continue;
-        int idx = 0;   // items of smaller experts
-        for (int f = 0; f < e; ++f) idx += sm.emask[f] != 0;
+    if (tid < kMaxExperts && sm.emask[tid] != 0) {
+        const int w = tid >> 5;
+        const int idx = (w ? __popc(sm.eball[0]) : 0) + __popc(sm.eball[w] & ((1u << (tid & 31)) - 1u));
+        sm.eidx[tid] = idx;
         Item& it = sm.items[idx];
-        it.expert = e;
-        it.mask = sm.emask[e];
+        it.expert = tid;
+        it.mask = sm.emask[tid];
         for (int t = 0; t < kMaxBlock; ++t) it.slot[t] = -1;
-        for (int i = 0; i < nk; ++i)
-            if ((ids[i] & 63) == e) it.slot[i / k] = (signed char)(i % k);
     }
+    __syncthreads();
+    for (int i = tid; i < nk; i += nthreads) sm.items[sm.eidx[ids[i] & 63]].slot[i / k] = (signed char)(i % k);
     if (tid == 0) {
-        int cnt = 0;
-        for (int e = 0; e < kMaxExperts; ++e) cnt += sm.emask[e] != 0;
+        const int cnt = __popc(sm.eball[0]) + __popc(sm.eball[1]);
         add_shared_items(p, sm, cnt);
         sm.n_items = cnt + p.n_shared;
     }
