@@ -183,8 +183,8 @@ __global__ void __maxnreg__(kMaxRegs) gemm_kernel(const __grid_constant__ GemmPa
             if constexpr (!kItems) {
                 // weights do not depend on the previous kernel: start streaming them now
                 int pre = 0;
-                int pre_b[kStages];
-                while (it.valid && pre < kStages) {
+                int pre_b[kPreStages];
+                while (it.valid && pre < kPreStages) {
                     mbar_arrive_expect_tx(&sm.full[pre], kStageWBytes + xb);
                     bulk_g2s(sm.w[pre], w_src(it), kStageWBytes, &sm.full[pre]);
                     pre_b[pre] = it.b;
