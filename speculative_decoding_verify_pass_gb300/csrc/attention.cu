@@ -335,28 +335,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_kernel(const __g
                 *reinterpret_cast<uint2*>(ph + off) = make_uint2(pack_bf16x2(hv[0], hv[1]), pack_bf16x2(hv[2], hv[3]));
                 *reinterpret_cast<uint2*>(pl + off) =
                     make_uint2(pack_bf16x2(pv[0] - hv[0], pv[1] - hv[1]), pack_bf16x2(pv[2] - hv[2], pv[3] - hv[3]));
-                if (qd == 0 && lane < 4) {   // per row: the merge weights and the running max
-                    const int c = 4 * q4 + lane;
-                    const float msj = lane == 0 ? ms[0] : lane == 1 ? ms[1] : lane == 2 ? ms[2] : ms[3];
-                    float w1 = 0.f, w2 = 1.f, mn = msj;
-                    if (accumulate) {   // maxima in the log2 domain
-                        const float mr = rowm[par][c];
-                        mn = fmaxf(mr, msj);
-                        w1 = ex2_approx(mr - mn);
-                        w2 = ex2_approx(msj - mn);
-                    }
-                    xw[c] = make_float2(w1, w2);
-                    rowm[par ^ 1][c] = mn;
-                }
             }
             fence_proxy_async_smem();   // P^T is read by the tensor core
             tc_fence_before();          // the S^T reads are done before the next S^T is written
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_ready);
+            named_bar_sync(1, 32 * kRowWarps);   // every quadrant's sums of P are in
+            const size_t prow = seq_base + ((size_t)h * p.nch + cur.x) * 64;   // the group's partial rows
+            if (tid < R) {
+                // one thread per row, while the O^T MMAs run (off the lane
+                // quadrants' loops, which would otherwise all wait for the
+                // warps that did this): the chunk's merge weights in the log2
+                // domain, the group's running max and running sum
+                const int c = tid;
+                const float M = fmaxf(fmaxf(xmax[0][c], xmax[1][c]), fmaxf(xmax[2][c], xmax[3][c]));
+                const float msj = M == -INFINITY ? -1e30f : M * k2;
+                float w1 = 0.f, w2 = 1.f, mn = msj;
+                if (accumulate) {
+                    const float mr = rowm[par][c];
+                    mn = fmaxf(mr, msj);
+                    w1 = ex2_approx(mr - mn);
+                    w2 = ex2_approx(msj - mn);
+                }
+                xw[c] = make_float2(w1, w2);
+                const float lc = (float)(xl[0][c] + xl[1][c] + xl[2][c] + xl[3][c]) * (1.f / kFix);
+                const float ln = accumulate ? rowl[par][c] * w1 + lc * w2 : lc;
+                if (flush) p.part_ml[prow + c] = make_float2(mn, ln);
+                rowm[par ^ 1][c] = mn;
+                rowl[par ^ 1][c] = ln;
+            }
             ok = ok && wait_bar(&o_done, i & 1, err, 25);
             tc_fence_after();
-            named_bar_sync(1, 32 * kRowWarps);   // this chunk's weights and sums are in
-            const size_t prow = seq_base + ((size_t)h * p.nch + cur.x) * 64;   // the group's partial rows
+            named_bar_sync(1, 32 * kRowWarps);   // this chunk's weights are in
 #pragma unroll 1
             for (int q4 = hc; q4 < nquad; q4 += 4) {   // merge into the group's running O, or write it out
                 if (dims) {
@@ -378,19 +388,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_partial_kernel(const __g
                             if (4 * q4 + j < R) p.part_o[(prow + 4 * q4 + j) * HD + d] = o[j];
                     } else {
                         tmem_st4(tl + kColRun + 4 * q4, o);
-                    }
-                }
-                if (qd == 0 && lane < 4) {   // per row: the running sum
-                    {
-                        const int c = 4 * q4 + lane;
-                        const float lc = (float)(xl[0][c] + xl[1][c] + xl[2][c] + xl[3][c]) * (1.f / kFix);
-                        const float2 w = xw[c];
-                        const float ln = accumulate ? rowl[par][c] * w.x + lc * w.y : lc;
-                        if (flush) {
-                            if (c < R) p.part_ml[prow + c] = make_float2(rowm[par ^ 1][c], ln);
-                        } else {
-                            rowl[par ^ 1][c] = ln;
-                        }
                     }
                 }
             }
