@@ -20,12 +20,15 @@
 //    visible keys is exact (an integer warp reduction, then across the four
 //    lane quadrants); P = exp2(S*scale*log2e - max) is kept as a bf16 high
 //    part plus a bf16 low part (~16 significant bits) and written as P^T, an
-//    MN-major operand (8 query rows of one key per 16-byte store);
+//    MN-major operand (a 16-byte core-matrix row holds one key's 8 query
+//    rows; each column quad of 4 rows writes half of one);
 //  * the row sum of P is exact in 24-bit fixed point (each P rounded to a
 //    multiple of 2^-24, integer sums over the warp and the four quadrants),
 //    so it is the same whatever the order of the terms;
 //  * the issuing thread runs O^T = V^T P^T (M = head dims, N as above, K = 128
 //    keys, high part then low part) into tensor memory;
+//  * while those MMAs run, one thread per query row takes the row's merge
+//    weights, running max and running sum;
 //  * every head dimension's thread merges O into the running partial of the
 //    chunk group (in tensor memory) or, for the group's last chunk, writes
 //    the group's unnormalised O and, per row, (max, sum) to global memory; a
