@@ -243,6 +243,75 @@ def test_gqa_ragged_vocab_synthetic_context(torch, ctx, n):
     argmax_mismatches(am.cpu().numpy(), ref)
 
 
+def many_kv_cfg():
+    """32 kv heads of 2 query heads each.  The attention unit makes about
+    SMs / kv heads chunk groups per kv head (5 on 152 SMs), so at contexts of
+    several hundred positions each group merges several 128-position chunks:
+    the running max, running sum and running O of a group are carried across
+    chunks, which the smaller models (one chunk per group) never do."""
+    return synth.ModelConfig("gqa-many-kv", 2, 256, 64, 32, 64, 512, 1000, rope_theta=5e5,
+                             max_ctx=2048, index=7)
+
+
+def _chunks_per_group(torch, cfg, total):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = min(-(-sms // cfg.n_kv_heads), cfg.max_ctx // 128)
+    return -(-(-(-total // 128)) // groups)
+
+
+def _load_synthetic_context(m, cfg, ctx, oc=None):
+    for l in range(cfg.n_layers):
+        k = synth.synthetic_kv(cfg, l, ctx, 0)
+        v = synth.synthetic_kv(cfg, l, ctx, 1)
+        m.kv_load(0, l, k, v)
+        if oc is not None:
+            oc.load(l, k.reshape(ctx, -1), v.reshape(ctx, -1))
+    m.kv_set_len(0, ctx)
+    if oc is not None:
+        oc.set_len(ctx)
+
+
+@pytest.mark.parametrize("ctx,n", [(700, 3), (1000, 16), (1900, 8)])
+def test_multichunk_groups_match_oracle(torch, ctx, n):
+    """Chunk groups of two and three chunks (running max, sum and O carried
+    across chunks, both parities of the per-row state) against the oracle at
+    the stated tolerance."""
+    cfg = many_kv_cfg()
+    assert _chunks_per_group(torch, cfg, ctx + n) >= 2
+    w = synth.make_weights(cfg)
+    m = make_model(cfg, w)
+    orc = oracle.Oracle(cfg, w)
+    oc = orc.new_cache()
+    _load_synthetic_context(m, cfg, ctx, oc)
+    toks = synth.prompt(cfg, n, stream=ctx)
+    am, _, lg, _ = m.verify(torch.tensor(toks, dtype=torch.int32, device="cuda"), logits=True)
+    ref, _, _ = orc.forward(oc, orc.full_plan, toks, ctx)
+    assert_logits_close(lg.cpu().numpy(), ref, "many-kv ctx=%d n=%d" % (ctx, n))
+    argmax_mismatches(am.cpu().numpy(), ref)
+    m.close()
+
+
+def test_multichunk_groups_rows_equal_decode_steps_bitwise(torch):
+    """Batch invariance where every chunk group merges two chunks: a block of
+    16 against one-token decode steps, bit for bit."""
+    cfg = many_kv_cfg()
+    ctx = 1100
+    assert _chunks_per_group(torch, cfg, ctx + 16) >= 2
+    w = synth.make_weights(cfg)
+    a = make_model(cfg, w)
+    b = make_model(cfg, w)
+    _load_synthetic_context(a, cfg, ctx)
+    _load_synthetic_context(b, cfg, ctx)
+    block = torch.tensor(synth.prompt(cfg, 16, stream=3), dtype=torch.int32, device="cuda")
+    am, _, lg, _ = a.verify(block, logits=True)
+    for j in range(16):
+        amj, _, lgj, _ = b.verify(block[j:j + 1].clone(), logits=True)
+        assert torch.equal(lg[j], lgj[0]), j
+        assert int(am[j]) == int(amj[0])
+    a.close()
+    b.close()
+
+
 def test_moe_small_matches_oracle_and_modes_agree(torch):
     import speculative_decoding_verify_pass_gb300 as sv
     cfg = small_moe_cfg()
