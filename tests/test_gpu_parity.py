@@ -312,6 +312,30 @@ def test_multichunk_groups_rows_equal_decode_steps_bitwise(torch):
     b.close()
 
 
+@pytest.mark.parametrize("hd,kv,ctx,n", [(64, 2, 3000, 5), (64, 2, 4000, 16), (128, 4, 3600, 8)])
+def test_merge_of_more_groups_than_its_first_sweep(torch, hd, kv, ctx, n):
+    """Few kv heads and a long context: a row has more chunk groups (24, 32,
+    29) than the merge kernel loads in its first sweep (20), so the later
+    groups go through its batches of eight (one, two and two batches, the
+    last one partial), for head dims 64 and 128."""
+    cfg = synth.ModelConfig("gqa-long-%d" % hd, 2, 256, 4 * kv, kv, hd, 512, 1000, rope_theta=5e5,
+                            max_ctx=4224, index=8)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    groups = min(-(-sms // kv), -(-cfg.max_ctx // 128))
+    assert min(groups, -(-(ctx + n) // 128)) > 20
+    w = synth.make_weights(cfg)
+    m = make_model(cfg, w)
+    orc = oracle.Oracle(cfg, w)
+    oc = orc.new_cache()
+    _load_synthetic_context(m, cfg, ctx, oc)
+    toks = synth.prompt(cfg, n, stream=ctx)
+    am, _, lg, _ = m.verify(torch.tensor(toks, dtype=torch.int32, device="cuda"), logits=True)
+    ref, _, _ = orc.forward(oc, orc.full_plan, toks, ctx)
+    assert_logits_close(lg.cpu().numpy(), ref, "long hd=%d ctx=%d n=%d" % (hd, ctx, n))
+    argmax_mismatches(am.cpu().numpy(), ref)
+    m.close()
+
+
 def test_moe_small_matches_oracle_and_modes_agree(torch):
     import speculative_decoding_verify_pass_gb300 as sv
     cfg = small_moe_cfg()
